@@ -1,0 +1,193 @@
+/*
+ * ekv.h -- C ABI of the ekv library: mixed-fidelity paged KV attention on GB300.
+ *
+ * Three operations, from the pages' statement of the problem:
+ *
+ *  - ekv_paged_decode: paged GQA decode attention that reads the mixed-fidelity KV
+ *    cache directly. Keys are FP16; each value page is TARGET (FP16) or compact
+ *    (FP8 E4M3 codes times a scale). ElasticKV ("Does Execution Require Target KV
+ *    Fidelity?"), Sec. 3.2 "Dual-mode Elastic Attention Backend": both fidelities are
+ *    consumed directly behind one attention interface, the compact state is expanded
+ *    in registers and never materialised, and TARGET-only batches keep the native
+ *    path. knlp.io "Asymmetric K16/V8 KV cache", Fig. "Fresh prefill gets a fast path
+ *    inside a mixed batch": the decode prefix reads persistent FP16 keys and FP8
+ *    values, and existing value scales still apply in attention.
+ *  - ekv_gather_prefill: compact prefill gathers stored K16/V8 pages into one bounded
+ *    FP16 workspace for a native FP16 prefill, casting V8 -> FP16 (knlp.io, "What
+ *    changes in vLLM's prefill routing?"; at most 4,096 pages, 256 MiB payload).
+ *  - ekv_demote_pages: TARGET -> compact demotion, synchronous and in place on the
+ *    GPU, the new state visible only after completion (ElasticKV Sec. 3.4
+ *    "Transition protocols"), requantising FP16 value pages to E4M3 with one absmax
+ *    scale per (page, KV head).
+ *
+ * Conventions for every entry point:
+ *  - Data pointers are DEVICE pointers owned by the caller, unless stated otherwise.
+ *    The library never frees or keeps them beyond the call.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Work is enqueued on it
+ *    and the call returns without synchronising. Hot calls allocate nothing.
+ *  - Argument errors are found on the host and returned before anything is launched.
+ *  - Errors found by the kernels (a page id outside the pool, a non-finite or <= 0
+ *    scale, a seq_len above the block table's capacity, a demotion page holding
+ *    NaN/inf, a timed-out pipeline wait) set a sticky error word in the context; the
+ *    affected outputs are zeroed (decode) or left untouched (demote). Read and clear it
+ *    with ekv_get_error.
+ *  - A context is bound to the device current at ekv_create and to one stream at a
+ *    time: calls that overlap on different streams race on its scratch.
+ *
+ * Page layout (NHD, page size 16, knlp.io measured route: "NHD layout, page size 16"):
+ *  - K pool: fp16 [num_pages][16][H_kv][D], contiguous.
+ *  - V pool: bytes [num_pages][v_page_stride_bytes]. A TARGET page holds fp16
+ *    [16][H_kv][D] in its first 16*H_kv*D*2 bytes; a compact page holds E4M3 codes
+ *    [16][H_kv][D] in its first 16*H_kv*D bytes. A uniform compact pool may use
+ *    stride 16*H_kv*D; a pool that holds TARGET pages needs stride >= 16*H_kv*D*2.
+ *    The stride must be a multiple of 16 bytes.
+ *  - Supported: H_kv in {1,2,4,8}, G = H_q/H_kv in {1..8}, D in {64,128}.
+ */
+#ifndef EKV_H
+#define EKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EKV_OK = 0,
+  EKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size/stride/enum, misaligned pointer */
+  EKV_ERR_UNSUPPORTED = 2,   /* shape outside the supported set: take your existing path */
+  EKV_ERR_CAPACITY = 3,      /* more pages than the workspace / context was sized for */
+  EKV_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, allocation, ...) */
+  EKV_ERR_DEVICE_CHECK = 5   /* a kernel found bad data (see ekv_get_error detail) */
+} ekv_status;
+
+/* Per-page value fidelity, one uint8 per physical page. */
+typedef enum { EKV_MODE_TARGET_FP16 = 0, EKV_MODE_COMPACT_E4M3 = 1 } ekv_page_mode;
+
+/* Granularity of the compact-page value scales (fp32, device memory).
+ * PER_TENSOR: v_scales[0] applies to every compact page (a per-layer scale is one
+ * per-tensor scale per call). PER_PAGE_HEAD: v_scales[p * H_kv + h]. */
+typedef enum { EKV_SCALE_PER_TENSOR = 0, EKV_SCALE_PER_PAGE_HEAD = 1 } ekv_scale_mode;
+
+/* Detail codes reported with EKV_ERR_DEVICE_CHECK by ekv_get_error. */
+typedef enum {
+  EKV_DETAIL_NONE = 0,
+  EKV_DETAIL_PAGE_ID = 1,        /* block_table / page_ids entry outside [0, num_pages) */
+  EKV_DETAIL_SCALE = 2,          /* a scale read by a compact page is NaN, inf or <= 0 */
+  EKV_DETAIL_SEQ_LEN = 3,        /* seq_lens[b] < 0 or > block_table_stride * 16 */
+  EKV_DETAIL_NONFINITE_PAGE = 4, /* a page given to demotion holds NaN or inf */
+  EKV_DETAIL_TIMEOUT = 5,        /* a bounded pipeline wait gave up */
+  EKV_DETAIL_PAGE_MODE = 6       /* a page_mode byte is neither TARGET nor COMPACT */
+} ekv_detail;
+
+typedef struct ekv_ctx ekv_ctx;
+
+typedef struct {
+  int num_q_heads;        /* H_q */
+  int num_kv_heads;       /* H_kv; H_q % H_kv == 0 */
+  int head_dim;           /* D: 64 or 128 */
+  int max_batch;          /* largest `batch` a decode call may pass (sizes the scratch) */
+} ekv_config;
+
+/* Create a context on the current device: allocates the split-K partials, the plan
+ * buffer and the sticky error word once (cudaMalloc). Returns EKV_ERR_UNSUPPORTED for
+ * shapes outside the supported set. *ctx is NULL on failure. */
+ekv_status ekv_create(ekv_ctx** ctx, const ekv_config* cfg);
+
+/* Free the context's device memory (synchronises the device first). NULL is a no-op. */
+ekv_status ekv_destroy(ekv_ctx* ctx);
+
+/* Paged GQA decode attention: for every sequence b and query head h_q,
+ *   out[b][h_q] = sum_t softmax_t(sm_scale * q[b][h_q] . k_t) v_t
+ * over the seq_lens[b] tokens of b, token t at page block_table[b][t/16], row t%16,
+ * KV head h_q / G; v_t is the FP16 row of a TARGET page or E4M3(code) * scale of a
+ * compact page. One query per sequence attends to all its cached tokens (no mask).
+ *
+ *  q            fp16 [batch][H_q][D], contiguous.
+ *  k_pages      fp16 [num_pages][16][H_kv][D]; 16-byte aligned.
+ *  v_pages      bytes [num_pages][v_page_stride_bytes]; 16-byte aligned.
+ *  v_scales     fp32, see ekv_scale_mode; may be NULL only if no page is compact.
+ *  page_mode    uint8 [num_pages] or NULL; NULL means every page has `uniform_mode`
+ *               (the uniform paths load no mode bytes; uniform TARGET loads no scales).
+ *  block_table  int32 [batch][block_table_stride]; entries past a sequence's pages
+ *               are not read.
+ *  seq_lens     int32 [batch]; 0 gives out = 0 and lse = -inf.
+ *  sm_scale     softmax scale; <= 0 means 1/sqrt(D).
+ *  out          fp16 [batch][H_q][D] (written).
+ *  lse          fp32 [batch][H_q] natural-log log-sum-exp of the scaled scores, or NULL.
+ * Returns EKV_ERR_CAPACITY when batch > cfg.max_batch. */
+ekv_status ekv_paged_decode(ekv_ctx* ctx, const void* q, const void* k_pages,
+                            const void* v_pages, long long v_page_stride_bytes,
+                            int num_pages, const float* v_scales, int scale_mode,
+                            const uint8_t* page_mode, int uniform_mode,
+                            const int32_t* block_table, int block_table_stride,
+                            const int32_t* seq_lens, int batch, float sm_scale,
+                            void* out, float* lse, void* stream);
+
+/* Compact-prefill gather: copies the pages named by `page_range` into consecutive
+ * workspace slots, in page_range order.
+ *
+ *  page_range   HOST int32 [n][3] rows {seq, first_page, num_pages}: logical pages
+ *               first_page .. first_page+num_pages-1 of sequence `seq`, reached through
+ *               block_table[seq]. 0 <= seq < block_table_rows and
+ *               first_page + num_pages <= block_table_stride are checked on the host.
+ *  ws_k, ws_v   fp16 [ws_pages][16][H_kv][D]: ws_k[w] = K page bit for bit; ws_v[w] =
+ *               the TARGET page bit for bit, or fp16_rn(fp32_rn(E4M3(code) * scale))
+ *               for a compact page (fp16(E4M3(code)) when apply_scale == 0).
+ *  ws_indices   int32 [ws_pages]: ws_indices[w] = w for every gathered page, the
+ *               workspace page table an FP16 prefill reads.
+ * Returns EKV_ERR_CAPACITY when the total page count exceeds ws_pages (nothing is
+ * launched). Other layout arguments are as for ekv_paged_decode. */
+ekv_status ekv_gather_prefill(ekv_ctx* ctx, const void* k_pages, const void* v_pages,
+                              long long v_page_stride_bytes, int num_pages,
+                              const float* v_scales, int scale_mode,
+                              const uint8_t* page_mode, int uniform_mode,
+                              const int32_t* block_table, int block_table_stride,
+                              int block_table_rows, const int32_t* page_range, int n,
+                              void* ws_k, void* ws_v, int32_t* ws_indices, int ws_pages,
+                              int apply_scale, void* stream);
+
+/* TARGET -> compact demotion, in place. For each page p = page_ids[i] whose
+ * page_mode[p] is TARGET, and each KV head h:
+ *   a = max |x| over the page's 16 x D fp16 values of head h,
+ *   s = fp32_rn(a / 448) (1.0 when a == 0),  code = E4M3_rn_satfinite(fp32_rn(x / s)),
+ * writes the codes into the first 16*H_kv*D bytes of the page's value slot,
+ * scale_out[p * H_kv + h] = s, then page_mode[p] = COMPACT. Pages that are not TARGET
+ * are skipped; a page holding NaN/inf is left TARGET and reported
+ * (EKV_DETAIL_NONFINITE_PAGE).
+ *  v_pages      bytes [num_pages][v_page_stride_bytes], stride >= 16*H_kv*D*2.
+ *  page_ids     int32 [n], distinct (duplicates race on the same page).
+ *  page_mode    uint8 [num_pages] (read and written).
+ *  scale_out    fp32 [num_pages][H_kv] (written for demoted pages).
+ * No decode or gather may read these pages concurrently on another stream. */
+ekv_status ekv_demote_pages(ekv_ctx* ctx, void* v_pages, long long v_page_stride_bytes,
+                            int num_pages, const int32_t* page_ids, int n,
+                            uint8_t* page_mode, float* scale_out, void* stream);
+
+/* Synchronise the stream of the context's last call, read the sticky device error
+ * word and clear it. *code is an ekv_status (EKV_OK or EKV_ERR_DEVICE_CHECK), *detail
+ * an ekv_detail. Either pointer may be NULL. Returns EKV_ERR_CUDA if the sync fails. */
+ekv_status ekv_get_error(ekv_ctx* ctx, int* code, int* detail);
+
+/* Kernel timing for measurement: when enabled, each ekv_paged_decode records CUDA
+ * events around its split-K kernel on the launching stream. ekv_profile_read
+ * synchronises, returns the summed split-kernel time in milliseconds and the number
+ * of timed launches since the last read, and resets both. */
+ekv_status ekv_profile_enable(ekv_ctx* ctx, int enable);
+ekv_status ekv_profile_read(ekv_ctx* ctx, double* split_ms, long long* launches);
+
+/* Decode consumer variant of this context: 0 (default) multiplies the QK and PV
+ * tiles on the tensor cores (mma.sync f16 -> f32); 1 uses CUDA-core FP32 FMAs. Both
+ * share the page pipeline and compute the same function; 1 exists for measurement. */
+ekv_status ekv_set_decode_variant(ekv_ctx* ctx, int variant);
+
+/* Number of SMs and split-K CTAs per decode launch the context uses. */
+ekv_status ekv_query(ekv_ctx* ctx, int* num_sms, int* split_ctas);
+
+/* Static string for a status code. */
+const char* ekv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EKV_H */

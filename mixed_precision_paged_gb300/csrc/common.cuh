@@ -1,0 +1,123 @@
+// common.cuh -- shared device helpers of the ekv kernels (sm_103a).
+//
+// mbarrier + TMA (cp.async.bulk.tensor) wrappers written as inline PTX, the shared
+// memory swizzle that TMA applies, bounded waits and the sticky error word.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/ekv.h"
+
+namespace ekv {
+
+constexpr int kPage = 16;                 // tokens per page (page size 16)
+constexpr int kMaxKvHeads = 8;
+constexpr int kMaxBatch = 4096;
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;   // 1 s bound on every pipeline wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- sticky error word
+// err[0] = ekv_status, err[1] = ekv_detail, err[2] = first offending index.
+__device__ __forceinline__ void report_error(int* err, int code, int detail, int index) {
+  if (atomicCAS(err, 0, code) == 0) {
+    err[1] = detail;
+    err[2] = index;
+  }
+}
+
+// ----------------------------------------------------------------------- mbarriers
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; gives up after kWaitTimeoutNs and
+// returns false (the caller then reports EKV_DETAIL_TIMEOUT and winds down).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
+// --------------------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+// 4-D tiled bulk tensor load global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm, int c0, int c1,
+                                            int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Byte offset inside a 1024-byte-aligned TMA box after the hardware swizzle:
+// 128B mode XORs the 16-byte chunk index (bits 4..6) with bits 7..9, 64B mode XORs
+// bits 4..5 with bits 7..8.
+__device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
+__device__ __forceinline__ uint32_t swz64(uint32_t off) { return off ^ (((off >> 7) & 3u) << 4); }
+
+// ----------------------------------------------------------------- conversions
+// Two E4M3 codes (low byte = first element) -> two fp16 values, exact.
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint16_t two_codes) {
+  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes), __NV_E4M3);
+  return *reinterpret_cast<__half2*>(&r);
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two_codes) {
+  return __half22float2(e4m3x2_to_half2(two_codes));
+}
+
+// Round two fp32 values to E4M3 (RN, saturating to +-448); low byte = x.
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float x, float y) {
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(x, y), __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ bool scale_ok(float s) { return s > 0.f && s <= 3.0e38f; }
+
+}  // namespace ekv

@@ -1,0 +1,397 @@
+// ekv_api.cu -- the C ABI (include/ekv.h): argument checks, tensor maps, launches.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "decode.cuh"
+#include "gather_demote.cuh"
+
+namespace ekv {
+size_t split_smem_bytes(int D, int vmode, int algo, int batch);
+cudaError_t launch_split_simt(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
+                              const DecodeParams& p, int D, int vmode, int grid, cudaStream_t st);
+cudaError_t launch_split_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
+                             const DecodeParams& p, int D, int vmode, int grid, cudaStream_t st);
+cudaError_t launch_merge(const DecodeParams& p, int D, cudaStream_t st);
+}  // namespace ekv
+
+using namespace ekv;
+
+struct ekv_ctx {
+  int device = 0;
+  int num_sms = 0;
+  int split_ctas = 0;
+  ekv_config cfg{};
+  int NG = 1;
+  int variant = 0;            // 0 tensor-core consumer, 1 CUDA-core consumer
+  float* part_acc = nullptr;
+  float2* part_ml = nullptr;
+  int* plan = nullptr;
+  int* err = nullptr;
+  cudaStream_t last_stream = nullptr;
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev;   // pairs (start, stop)
+  size_t ev_used = 0;            // pairs recorded since the last read
+  double prof_ms = 0.0;
+  long long prof_launches = 0;
+};
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D view (d, head, token-in-page, page) of a page pool; one box = 16 rows of one
+// KV head and `box_d` columns, landing [16][box_d * esz] in shared memory.
+bool encode_pool_map(CUtensorMap* tm, CUtensorMapDataType dt, int esz, const void* base, int D,
+                     int Hkv, int num_pages, long long page_stride, int box_d,
+                     CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)kPage, (cuuint64_t)num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)D * esz, (cuuint64_t)Hkv * D * esz, (cuuint64_t)page_stride};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)kPage, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(tm, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+    else prev = -1;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+bool supported_shape(int Hq, int Hkv, int D) {
+  if (D != 64 && D != 128) return false;
+  if (Hkv != 1 && Hkv != 2 && Hkv != 4 && Hkv != 8) return false;
+  if (Hq <= 0 || Hq % Hkv != 0) return false;
+  const int G = Hq / Hkv;
+  return G >= 1 && G <= 8;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ekv_status_string(int s) {
+  switch (s) {
+    case EKV_OK: return "EKV_OK";
+    case EKV_ERR_INVALID_ARG: return "EKV_ERR_INVALID_ARG";
+    case EKV_ERR_UNSUPPORTED: return "EKV_ERR_UNSUPPORTED";
+    case EKV_ERR_CAPACITY: return "EKV_ERR_CAPACITY";
+    case EKV_ERR_CUDA: return "EKV_ERR_CUDA";
+    case EKV_ERR_DEVICE_CHECK: return "EKV_ERR_DEVICE_CHECK";
+    default: return "EKV_UNKNOWN_STATUS";
+  }
+}
+
+ekv_status ekv_create(ekv_ctx** out, const ekv_config* cfg) {
+  if (!out) return EKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return EKV_ERR_INVALID_ARG;
+  if (cfg->max_batch < 1 || cfg->num_q_heads < 1 || cfg->num_kv_heads < 1 || cfg->head_dim < 1)
+    return EKV_ERR_INVALID_ARG;
+  if (!supported_shape(cfg->num_q_heads, cfg->num_kv_heads, cfg->head_dim) || cfg->max_batch > kMaxBatch)
+    return EKV_ERR_UNSUPPORTED;
+  ekv_ctx* c = new (std::nothrow) ekv_ctx();
+  if (!c) return EKV_ERR_CUDA;
+  c->cfg = *cfg;
+  c->NG = kConsumerWarps / cfg->num_kv_heads;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return EKV_ERR_CUDA;
+  }
+  c->split_ctas = c->num_sms;                     // one 288-thread CTA per SM (~200 KB smem)
+  const size_t records = (size_t)(cfg->max_batch + c->split_ctas) * c->NG;
+  const size_t hq = (size_t)cfg->num_q_heads;
+  bool ok = cudaMalloc(&c->part_acc, records * hq * cfg->head_dim * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&c->part_ml, records * hq * sizeof(float2)) == cudaSuccess &&
+            cudaMalloc(&c->plan, kPlanInts * sizeof(int)) == cudaSuccess &&
+            cudaMalloc(&c->err, 4 * sizeof(int)) == cudaSuccess &&
+            cudaMemset(c->plan, 0, kPlanInts * sizeof(int)) == cudaSuccess &&
+            cudaMemset(c->err, 0, 4 * sizeof(int)) == cudaSuccess &&
+            cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok || !get_encode()) {
+    ekv_destroy(c);
+    return EKV_ERR_CUDA;
+  }
+  *out = c;
+  return EKV_OK;
+}
+
+ekv_status ekv_destroy(ekv_ctx* c) {
+  if (!c) return EKV_OK;
+  DeviceGuard g(c->device);
+  cudaDeviceSynchronize();
+  for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
+  cudaFree(c->part_acc);
+  cudaFree(c->part_ml);
+  cudaFree(c->plan);
+  cudaFree(c->err);
+  delete c;
+  return EKV_OK;
+}
+
+ekv_status ekv_set_decode_variant(ekv_ctx* c, int variant) {
+  if (!c || (variant != 0 && variant != 1)) return EKV_ERR_INVALID_ARG;
+  c->variant = variant;
+  return EKV_OK;
+}
+
+ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, const void* v_pages,
+                            long long v_page_stride_bytes, int num_pages, const float* v_scales,
+                            int scale_mode, const uint8_t* page_mode, int uniform_mode,
+                            const int32_t* block_table, int block_table_stride,
+                            const int32_t* seq_lens, int batch, float sm_scale, void* out,
+                            float* lse, void* stream) {
+  if (!c) return EKV_ERR_INVALID_ARG;
+  if (batch < 0) return EKV_ERR_INVALID_ARG;
+  if (batch > c->cfg.max_batch) return EKV_ERR_CAPACITY;
+  if (batch == 0) return EKV_OK;
+  const int Hq = c->cfg.num_q_heads, Hkv = c->cfg.num_kv_heads, D = c->cfg.head_dim;
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out) return EKV_ERR_INVALID_ARG;
+  if (num_pages < 1 || block_table_stride < 1) return EKV_ERR_INVALID_ARG;
+  if (scale_mode != EKV_SCALE_PER_TENSOR && scale_mode != EKV_SCALE_PER_PAGE_HEAD) return EKV_ERR_INVALID_ARG;
+  if (uniform_mode != EKV_MODE_TARGET_FP16 && uniform_mode != EKV_MODE_COMPACT_E4M3) return EKV_ERR_INVALID_ARG;
+  const int vmode = page_mode ? kVMixed : (uniform_mode == EKV_MODE_COMPACT_E4M3 ? kVE4M3 : kVFP16);
+  const long long n_elem = (long long)kPage * Hkv * D;
+  const long long need = vmode == kVE4M3 ? n_elem : 2 * n_elem;
+  if (v_page_stride_bytes < need || (v_page_stride_bytes & 15)) return EKV_ERR_INVALID_ARG;
+  if (vmode != kVFP16 && !v_scales) return EKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return EKV_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return EKV_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !isfinite(sm_scale)) sm_scale = 1.0f / sqrtf((float)D);
+
+  DeviceGuard g(c->device);
+  CUtensorMap tk, t8, t16;
+  memset(&tk, 0, sizeof(tk));
+  memset(&t8, 0, sizeof(t8));
+  memset(&t16, 0, sizeof(t16));
+  if (!encode_pool_map(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, k_pages, D, Hkv, num_pages,
+                       (long long)kPage * Hkv * D * 2, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return EKV_ERR_INVALID_ARG;
+  if (vmode != kVFP16 &&
+      !encode_pool_map(&t8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, v_pages, D, Hkv, num_pages, v_page_stride_bytes, D,
+                       D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+    return EKV_ERR_INVALID_ARG;
+  if (vmode != kVE4M3 &&
+      !encode_pool_map(&t16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, v_pages, D, Hkv, num_pages, v_page_stride_bytes,
+                       64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return EKV_ERR_INVALID_ARG;
+
+  DecodeParams p;
+  p.q = static_cast<const __half*>(q);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.page_mode = page_mode;
+  p.v_scales = v_scales;
+  p.part_acc = c->part_acc;
+  p.part_ml = c->part_ml;
+  p.plan = c->plan;
+  p.err = c->err;
+  p.out = static_cast<__half*>(out);
+  p.lse = lse;
+  p.bt_stride = block_table_stride;
+  p.batch = batch;
+  p.num_pages = num_pages;
+  p.uniform_mode = uniform_mode;
+  p.scale_mode = scale_mode;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.NG = c->NG;
+  p.qscale = sm_scale * 1.4426950408889634f;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  c->last_stream = st;
+  const bool timed = c->profiling && c->ev_used * 2 + 1 < c->ev.size();
+  if (timed) cudaEventRecord(c->ev[2 * c->ev_used], st);
+  cudaError_t e = c->variant == 1 ? launch_split_simt(tk, t8, t16, p, D, vmode, c->split_ctas, st)
+                                  : launch_split_mma(tk, t8, t16, p, D, vmode, c->split_ctas, st);
+  if (e != cudaSuccess) return EKV_ERR_CUDA;
+  if (timed) {
+    cudaEventRecord(c->ev[2 * c->ev_used + 1], st);
+    ++c->ev_used;
+  }
+  if (launch_merge(p, D, st) != cudaSuccess) return EKV_ERR_CUDA;
+  return EKV_OK;
+}
+
+ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pages,
+                              long long v_page_stride_bytes, int num_pages, const float* v_scales,
+                              int scale_mode, const uint8_t* page_mode, int uniform_mode,
+                              const int32_t* block_table, int block_table_stride, int block_table_rows,
+                              const int32_t* page_range, int n, void* ws_k, void* ws_v,
+                              int32_t* ws_indices, int ws_pages, int apply_scale, void* stream) {
+  if (!c || n < 0 || ws_pages < 0) return EKV_ERR_INVALID_ARG;
+  if (n == 0) return EKV_OK;
+  const int Hkv = c->cfg.num_kv_heads, D = c->cfg.head_dim;
+  if (!page_range || !k_pages || !v_pages || !block_table || !ws_k || !ws_v || !ws_indices)
+    return EKV_ERR_INVALID_ARG;
+  if (num_pages < 1 || block_table_stride < 1 || block_table_rows < 1) return EKV_ERR_INVALID_ARG;
+  if (scale_mode != EKV_SCALE_PER_TENSOR && scale_mode != EKV_SCALE_PER_PAGE_HEAD) return EKV_ERR_INVALID_ARG;
+  if (uniform_mode != EKV_MODE_TARGET_FP16 && uniform_mode != EKV_MODE_COMPACT_E4M3) return EKV_ERR_INVALID_ARG;
+  const bool any_compact = page_mode || uniform_mode == EKV_MODE_COMPACT_E4M3;
+  const bool any_target = page_mode || uniform_mode == EKV_MODE_TARGET_FP16;
+  const long long n_elem = (long long)kPage * Hkv * D;
+  if (v_page_stride_bytes < (any_target ? 2 * n_elem : n_elem) || (v_page_stride_bytes & 15))
+    return EKV_ERR_INVALID_ARG;
+  if (any_compact && apply_scale && !v_scales) return EKV_ERR_INVALID_ARG;
+  if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(ws_k) || !aligned16(ws_v))
+    return EKV_ERR_INVALID_ARG;
+  long long total = 0;
+  for (int i = 0; i < n; ++i) {
+    const int seq = page_range[3 * i], first = page_range[3 * i + 1], num = page_range[3 * i + 2];
+    if (seq < 0 || seq >= block_table_rows || first < 0 || num < 0 ||
+        (long long)first + num > block_table_stride)
+      return EKV_ERR_INVALID_ARG;
+    total += num;
+  }
+  if (total > ws_pages) return EKV_ERR_CAPACITY;
+
+  DeviceGuard g(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  c->last_stream = st;
+  GatherParams p;
+  p.k_pages = static_cast<const __half*>(k_pages);
+  p.v_pages = static_cast<const uint8_t*>(v_pages);
+  p.v_page_stride = v_page_stride_bytes;
+  p.num_pages = num_pages;
+  p.v_scales = v_scales;
+  p.scale_mode = scale_mode;
+  p.page_mode = page_mode;
+  p.uniform_mode = uniform_mode;
+  p.block_table = block_table;
+  p.bt_stride = block_table_stride;
+  p.ws_k = static_cast<__half*>(ws_k);
+  p.ws_v = static_cast<__half*>(ws_v);
+  p.ws_indices = ws_indices;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.apply_scale = apply_scale ? 1 : 0;
+  p.err = c->err;
+  int base = 0;
+  for (int i0 = 0; i0 < n; i0 += kMaxRanges) {
+    GatherRanges r;
+    memset(&r, 0, sizeof(r));
+    r.n = n - i0 < kMaxRanges ? n - i0 : kMaxRanges;
+    int off = 0;
+    for (int k = 0; k < r.n; ++k) {
+      r.seq[k] = page_range[3 * (i0 + k)];
+      r.first[k] = page_range[3 * (i0 + k) + 1];
+      r.off[k] = off;
+      off += page_range[3 * (i0 + k) + 2];
+    }
+    r.off[r.n] = off;
+    p.ws_base = base;
+    if (launch_gather(p, r, off, st) != cudaSuccess) return EKV_ERR_CUDA;
+    base += off;
+  }
+  return EKV_OK;
+}
+
+ekv_status ekv_demote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_bytes, int num_pages,
+                            const int32_t* page_ids, int n, uint8_t* page_mode, float* scale_out,
+                            void* stream) {
+  if (!c || n < 0) return EKV_ERR_INVALID_ARG;
+  if (n == 0) return EKV_OK;
+  const int Hkv = c->cfg.num_kv_heads, D = c->cfg.head_dim;
+  if (!v_pages || !page_ids || !page_mode || !scale_out || num_pages < 1) return EKV_ERR_INVALID_ARG;
+  const long long n_elem = (long long)kPage * Hkv * D;
+  if (v_page_stride_bytes < 2 * n_elem || (v_page_stride_bytes & 15) || !aligned16(v_pages))
+    return EKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  c->last_stream = st;
+  DemoteParams p;
+  p.v_pages = static_cast<uint8_t*>(v_pages);
+  p.v_page_stride = v_page_stride_bytes;
+  p.num_pages = num_pages;
+  p.page_ids = page_ids;
+  p.page_mode = page_mode;
+  p.scale_out = scale_out;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.err = c->err;
+  return launch_demote(p, n, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+}
+
+ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {
+  if (!c) return EKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (cudaStreamSynchronize(c->last_stream) != cudaSuccess) return EKV_ERR_CUDA;
+  int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, c->err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return EKV_ERR_CUDA;
+  if (cudaMemset(c->err, 0, sizeof(h)) != cudaSuccess) return EKV_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return EKV_ERR_CUDA;
+  if (code) *code = h[0];
+  if (detail) *detail = h[1];
+  return EKV_OK;
+}
+
+ekv_status ekv_profile_enable(ekv_ctx* c, int enable) {
+  if (!c) return EKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (enable && c->ev.empty()) {
+    c->ev.resize(2 * 8192);
+    for (auto& e : c->ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return EKV_ERR_CUDA;
+  }
+  c->profiling = enable != 0;
+  return EKV_OK;
+}
+
+ekv_status ekv_profile_read(ekv_ctx* c, double* split_ms, long long* launches) {
+  if (!c) return EKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  double ms = 0.0;
+  for (size_t i = 0; i < c->ev_used; ++i) {
+    if (cudaEventSynchronize(c->ev[2 * i + 1]) != cudaSuccess) return EKV_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, c->ev[2 * i], c->ev[2 * i + 1]) != cudaSuccess) return EKV_ERR_CUDA;
+    ms += t;
+  }
+  if (split_ms) *split_ms = ms;
+  if (launches) *launches = (long long)c->ev_used;
+  c->ev_used = 0;
+  return EKV_OK;
+}
+
+ekv_status ekv_query(ekv_ctx* c, int* num_sms, int* split_ctas) {
+  if (!c) return EKV_ERR_INVALID_ARG;
+  if (num_sms) *num_sms = c->num_sms;
+  if (split_ctas) *split_ctas = c->split_ctas;
+  return EKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+"""GPU parity of ekv_gather_prefill and ekv_demote_pages: bit-exact against the oracle."""
+
+import numpy as np
+import pytest
+
+from mixed_precision_paged_gb300 import workloads as wl
+from oracle import demote as odm
+from oracle import gather as og
+
+from _helpers import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+def run_gather(ekv_lib, torch, case, page_range, ws_pages, apply_scale=1):
+    d = to_device(case)
+    H, D = case.num_kv_heads, case.head_dim
+    ws_k = torch.full((ws_pages, 16, H, D), float("nan"), dtype=torch.float16, device="cuda")
+    ws_v = torch.full((ws_pages, 16, H, D), float("nan"), dtype=torch.float16, device="cuda")
+    idx = torch.full((ws_pages,), -1, dtype=torch.int32, device="cuda")
+    ctx = ekv_lib.Context(case.num_q_heads, H, D, 1)
+    ekv_lib.ekv_gather_prefill(ctx.handle, d.k_pages, d.v_pages, case.v_page_stride, case.num_pages,
+                               d.v_scales, case.scale_mode, d.page_mode, case.uniform_mode,
+                               d.block_table, case.block_table.shape[1], case.batch, page_range,
+                               ws_k, ws_v, idx, ws_pages, apply_scale)
+    torch.cuda.synchronize()
+    assert ctx.error() == (0, 0)
+    return ws_k.cpu().numpy(), ws_v.cpu().numpy(), idx.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt,scale_mode,apply", [("e4m3", 0, 1), ("e4m3", 1, 1), ("mixed", 1, 1),
+                                                  ("fp16", 0, 1), ("e4m3", 1, 0), ("mixed", 0, 1)])
+@pytest.mark.parametrize("hkv,d", [(8, 128), (2, 64), (4, 128)])
+def test_gather_bit_exact(ekv_lib, torch_cuda, fmt, scale_mode, apply, hkv, d):
+    lens = [300, 40, 1000, 17]
+    case = wl.make_decode_case(lens, hkv * 2, hkv, d, v_format=fmt, scale_mode=scale_mode,
+                               pool_pages=sum((l + 15) // 16 for l in lens) + 4, seed=21, poison=False)
+    page_range = np.array([[2, 3, 40], [0, 0, 19], [3, 1, 1], [1, 0, 0], [2, 50, 13]])
+    total = int(page_range[:, 2].sum())
+    ws_k, ws_v, idx = run_gather(ekv_lib, torch_cuda, case, page_range, total + 3, apply)
+    rk, rv, ri = og.gather_prefill(case.k_pages, case.v_pages, case.v_scales, scale_mode,
+                                   case.page_mode, case.uniform_mode, case.block_table, page_range,
+                                   apply_scale=bool(apply))
+    assert np.array_equal(ws_k[:total].view(np.uint16), rk.view(np.uint16))
+    assert np.array_equal(ws_v[:total].view(np.uint16), rv.view(np.uint16))
+    assert np.array_equal(idx[:total], ri)
+    assert np.all(idx[total:] == -1)        # slots past the gathered pages untouched
+
+
+def test_gather_many_ranges_chunked(ekv_lib, torch_cuda):
+    lens = [16 * 3] * 300
+    case = wl.make_decode_case(lens, 8, 4, 64, v_format="mixed", scale_mode=1,
+                               pool_pages=900, seed=22, poison=False)
+    page_range = np.array([[s, s % 3, 1 + (s % 2)] for s in range(300)])
+    page_range[:, 2] = np.minimum(page_range[:, 2], 3 - page_range[:, 1])
+    total = int(page_range[:, 2].sum())
+    ws_k, ws_v, idx = run_gather(ekv_lib, torch_cuda, case, page_range, total)
+    rk, rv, ri = og.gather_prefill(case.k_pages, case.v_pages, case.v_scales, 1, case.page_mode,
+                                   0, case.block_table, page_range)
+    assert np.array_equal(ws_k.view(np.uint16), rk.view(np.uint16))
+    assert np.array_equal(ws_v.view(np.uint16), rv.view(np.uint16))
+    assert np.array_equal(idx, ri)
+
+
+def run_demote(ekv_lib, torch, vb, ids, mode, H, D):
+    v = torch.from_numpy(vb.copy()).cuda()
+    m = torch.from_numpy(mode.copy()).cuda()
+    sc = torch.zeros((vb.shape[0], H), dtype=torch.float32, device="cuda")
+    pid = torch.from_numpy(np.asarray(ids, dtype=np.int32)).cuda()
+    ctx = ekv_lib.Context(H, H, D, 1)
+    ekv_lib.ekv_demote_pages(ctx.handle, v, vb.shape[1], vb.shape[0], pid, len(ids), m, sc)
+    torch.cuda.synchronize()
+    err = ctx.error()
+    return v.cpu().numpy(), m.cpu().numpy(), sc.cpu().numpy(), err
+
+
+@pytest.mark.parametrize("hkv,d,std", [(8, 128, 2 ** 0.5), (2, 64, 1.0), (4, 128, 1e-3), (1, 64, 300.0)])
+def test_demote_bit_exact(ekv_lib, torch_cuda, hkv, d, std):
+    rng = np.random.default_rng(31)
+    P = 40
+    x = (rng.standard_normal((P, 16, hkv, d)) * std).astype(np.float16)
+    x[3] = 0
+    x[5, :, 0] = -x[5, :, 0]
+    vb = x.reshape(P, -1).view(np.uint8).copy()
+    mode = np.zeros(P, dtype=np.uint8)
+    mode[7] = 1                                   # already compact: skipped
+    ids = rng.permutation(P)[:20].tolist() + [7, 3]
+    v, m, sc, err = run_demote(ekv_lib, torch_cuda, vb, ids, mode, hkv, d)
+    rv, rm, rs = odm.demote_pages(vb, ids, mode, np.zeros((P, hkv), np.float32), hkv, d)
+    assert err == (0, 0)
+    assert np.array_equal(m, rm)
+    assert np.array_equal(v, rv)
+    demoted = [p for p in set(ids) if mode[p] == 0]
+    assert np.array_equal(sc[demoted], rs[demoted])
+
+
+def test_demote_then_gather_round_trip(ekv_lib, torch_cuda):
+    import torch
+    rng = np.random.default_rng(33)
+    P, H, D = 24, 8, 128
+    x = (rng.standard_normal((P, 16, H, D)) * 2 ** 0.5).astype(np.float16)
+    vb = x.reshape(P, -1).view(np.uint8).copy()
+    ids = rng.permutation(P)[:12]
+    v, m, sc, err = run_demote(ekv_lib, torch_cuda, vb, ids, np.zeros(P, np.uint8), H, D)
+    assert err == (0, 0)
+    case = wl.DecodeCase(q=None, k_pages=rng.standard_normal((P, 16, H, D)).astype(np.float16),
+                         v_pages=v, v_scales=sc, scale_mode=1, page_mode=m, uniform_mode=0,
+                         block_table=np.arange(P, dtype=np.int32)[None, :],
+                         seq_lens=np.array([16 * P], np.int32), num_q_heads=H, num_kv_heads=H,
+                         head_dim=D)
+    ws_k, ws_v, _ = run_gather(ekv_lib, torch, case, np.array([[0, 0, P]]), P)
+    rv2, rm2, rs2 = odm.demote_pages(vb, ids, np.zeros(P, np.uint8), np.zeros((P, H), np.float32), H, D)
+    _, ref_v, _ = og.gather_prefill(case.k_pages, rv2, rs2, 1, rm2, 0, case.block_table,
+                                    np.array([[0, 0, P]]))
+    assert np.array_equal(ws_v.view(np.uint16), ref_v.view(np.uint16))
+    for p in range(P):
+        if m[p] == 0:
+            assert np.array_equal(ws_v[p].view(np.uint16), x[p].view(np.uint16))
