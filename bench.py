@@ -1,0 +1,572 @@
+"""Benchmark of the paged K16/V8 decode hot path on GB300 (one JSON line on rank 0).
+
+Default workload: asymmetric-KV decode at the pages' shape -- batch 32, context
+8192 + U{0..127}, 32 query / 8 KV heads, head dim 128, page size 16, NHD pages, K FP16,
+V FP8 E4M3 with a per-layer scale, 36 layers per step (36 distinct layer pools, 29 GB,
+so every layer call streams from HBM: inputs larger than L2, no flush needed).
+A step is one decode call per layer (split kernel + merge kernel each).
+
+value        KV GB/s: algorithmic bytes of all layer calls / device time (CUDA events)
+e2e          the same metric through the C ABI with the per-step inputs (q, block
+             tables, seq_lens) copied host->device from pinned memory and the outputs
+             copied back inside the timed region (the KV cache is resident state)
+roofline     split kernel's algorithmic bytes / its own event-timed duration, against
+             the measured HBM copy peak
+cpu_baseline the float64 oracle on the host cores, on a sample of the same workload
+companions   gather + demotion on the 32 x 8192-token gather/demote workload
+
+--impl reference times the float64 oracle (the reference arm of this build) on the
+host cores, on bounded samples of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOADS = {
+    "pages_shape": dict(desc="asymmetric-KV decode at the pages' shape", batch=32, q_heads=32,
+                        kv_heads=8, head_dim=128, layers=36, v_format="e4m3", scale_mode=0,
+                        context="8192+U{0..127}"),
+    "high_concurrency": dict(desc="high-concurrency decode", batch=256, q_heads=32, kv_heads=4,
+                             head_dim=128, layers=48, v_format="e4m3", scale_mode=0,
+                             context="20% U[1,63], rest ceil(LogNormal(ln 2048, 1)) <= 32768"),
+    "mixed": dict(desc="mixed-fidelity batch", batch=64, q_heads=32, kv_heads=8, head_dim=128,
+                  layers=1, v_format="mixed", scale_mode=1, context="U[512, 32768]"),
+    "mixed_fp16_control": dict(desc="mixed-fidelity batch, all-FP16 control", batch=64, q_heads=32,
+                               kv_heads=8, head_dim=128, layers=1, v_format="fp16", scale_mode=0,
+                               context="U[512, 32768]"),
+}
+
+
+def lens_for(name):
+    from mixed_precision_paged_gb300 import workloads as wl
+    if name == "pages_shape":
+        return wl.pages_shape_lens()
+    if name == "high_concurrency":
+        return wl.high_concurrency_lens()
+    return wl.mixed_lens()
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ["decode_mma.cu", "pipeline.cuh", "decode.cuh", "common.cuh"]:
+        h.update(open(os.path.join(ROOT, "mixed_precision_paged_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per split launch from the committed ncu summary, when it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"decode_split_mma_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------- oracle (CPU)
+
+def _oracle_unit(args):
+    """One sequence through the float64 oracle (runs in a single-threaded worker)."""
+    from oracle import decode as od
+    q, k, v, scales, scale_mode, modes, uniform_mode, L = args
+    n = k.shape[0]
+    bt = np.arange(n, dtype=np.int32)[None, :]
+    out, lse = od.paged_decode(q[None], k, v, scales, scale_mode, modes, uniform_mode, bt,
+                               np.array([L], dtype=np.int32))
+    return out[0]
+
+
+def _init_worker():
+    os.environ["OMP_NUM_THREADS"] = "1"
+
+
+def oracle_pool(cores):
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    pool = ctx.Pool(cores, initializer=_init_worker)
+    os.environ.clear()
+    os.environ.update(env)
+    return pool
+
+
+def host_units(case_np, seqs):
+    """Per-sequence oracle inputs with the sequence's pages renumbered 0..n-1."""
+    units = []
+    for b in seqs:
+        L = int(case_np.seq_lens[b])
+        n = (L + 15) // 16
+        pages = case_np.block_table[b, :n]
+        scales = case_np.v_scales if case_np.scale_mode == 0 else case_np.v_scales[pages]
+        modes = None if case_np.page_mode is None else case_np.page_mode[pages]
+        units.append((case_np.q[b], case_np.k_pages[pages], case_np.v_pages[pages], scales,
+                      case_np.scale_mode, modes, case_np.uniform_mode, L))
+    return units
+
+
+def device_case_to_host(case, seqs):
+    """Host copies of the arrays the oracle needs for sequences `seqs` only."""
+    from mixed_precision_paged_gb300 import workloads as wl
+    import torch
+    bt = case.block_table.cpu().numpy()
+    lens = case.seq_lens.cpu().numpy()
+    need = sorted({int(p) for b in seqs for p in bt[b, : (int(lens[b]) + 15) // 16]})
+    remap = np.full(case.num_pages, -1, dtype=np.int64)
+    remap[need] = np.arange(len(need))
+    idx = torch.as_tensor(need, device=case.k_pages.device)
+    k = case.k_pages.index_select(0, idx).cpu().numpy()
+    v = case.v_pages.index_select(0, idx).cpu().numpy()
+    sc = case.v_scales.cpu().numpy() if case.scale_mode == 0 else case.v_scales.index_select(0, idx).cpu().numpy()
+    pm = None if case.page_mode is None else case.page_mode.index_select(0, idx).cpu().numpy()
+    bt2 = np.where(bt >= 0, remap[np.clip(bt, 0, case.num_pages - 1)], 0).astype(np.int32)
+    return wl.DecodeCase(q=case.q.cpu().numpy(), k_pages=k, v_pages=v, v_scales=sc,
+                         scale_mode=case.scale_mode, page_mode=pm, uniform_mode=case.uniform_mode,
+                         block_table=bt2, seq_lens=lens, num_q_heads=case.num_q_heads,
+                         num_kv_heads=case.num_kv_heads, head_dim=case.head_dim)
+
+
+def cpu_baseline(cases, wk, target_s=15.0):
+    """Time the oracle on whole sequences of the first layers until ~target_s of CPU
+    work has been sampled (one single-threaded spawn worker per host core)."""
+    from mixed_precision_paged_gb300 import roofline as rf
+    cores = os.cpu_count() or 1
+    pool = oracle_pool(cores)
+    try:
+        # calibrate on one sequence
+        c0 = device_case_to_host(cases[0], [0])
+        t0 = time.perf_counter()
+        pool.map(_oracle_unit, host_units(c0, [0]))
+        per_seq = time.perf_counter() - t0
+        n_seq_total = max(1, int(target_s / max(per_seq, 1e-3)))
+        units, lens = [], []
+        li = 0
+        while len(units) < n_seq_total and li < len(cases):
+            B = cases[li].batch
+            take = list(range(min(B, n_seq_total - len(units))))
+            hc = device_case_to_host(cases[li], take)
+            units += host_units(hc, take)
+            lens += [int(hc.seq_lens[b]) for b in take]
+            li += 1
+        t0 = time.perf_counter()
+        pool.map(_oracle_unit, units, chunksize=1)
+        wall = time.perf_counter() - t0
+    finally:
+        pool.close()
+        pool.join()
+    vb = 1 if wk["v_format"] == "e4m3" else 2
+    nbytes = rf.decode_bytes(lens, wk["q_heads"], wk["kv_heads"], wk["head_dim"], vb,
+                             per_page_scales=False)["total"] if wk["v_format"] != "mixed" else None
+    if nbytes is None:
+        nbytes = sum(l * wk["kv_heads"] * wk["head_dim"] * 3 for l in lens)
+    return {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(units)} whole sequences (layers 0..{li - 1}), float64 numpy oracle, "
+                      f"{cores} single-threaded spawn workers, {wall:.2f} s wall"}
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from mixed_precision_paged_gb300 import roofline as rf
+    from mixed_precision_paged_gb300 import workloads as wl
+    wk = WORKLOADS[args.workload]
+    cores = os.cpu_count() or 1
+    lens_all = lens_for(args.workload)
+    n = min(len(lens_all), cores)
+    lens = lens_all[:n]
+    case = wl.make_decode_case(lens, wk["q_heads"], wk["kv_heads"], wk["head_dim"],
+                               v_format=wk["v_format"], scale_mode=wk["scale_mode"],
+                               seed=args.seed, poison=False)
+    units = host_units(case, range(n))
+    vb = 1 if wk["v_format"] == "e4m3" else 2
+    nbytes = rf.decode_bytes(lens, wk["q_heads"], wk["kv_heads"], wk["head_dim"], vb,
+                             per_page_scales=False)["total"]
+    pool = oracle_pool(cores)
+    try:
+        for _ in range(args.warmup):
+            pool.map(_oracle_unit, units, chunksize=1)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            pool.map(_oracle_unit, units, chunksize=1)
+        wall = time.perf_counter() - t0
+    finally:
+        pool.close()
+        pool.join()
+    value = nbytes * args.steps / wall / 1e9
+    sample = (f"each step: {n} of the workload's sequences (one layer), float64 numpy oracle, "
+              f"{cores} single-threaded spawn workers")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(args, wk),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+METRIC = "paged K16/V8 decode attention: KV GB/s and % of GB300 HBM peak; tokens/s"
+
+
+def config_of(args, wk):
+    return {"workload": wk["desc"], "batch": wk["batch"], "context": wk["context"],
+            "q_heads": wk["q_heads"], "kv_heads": wk["kv_heads"], "head_dim": wk["head_dim"],
+            "page_size": 16, "layers": args.layers or wk["layers"],
+            "kv_format": {"e4m3": "K fp16 / V e4m3, per-layer scale",
+                          "fp16": "K fp16 / V fp16",
+                          "mixed": "K fp16 / V per page fp16 or e4m3 (p=0.5), per-(page, head) scale"}[wk["v_format"]],
+            "l2": "inputs larger than L2: distinct layer pools streamed in turn"
+                  if (args.layers or wk["layers"]) > 1 else "L2 flushed (1 GiB write) between steps",
+            "parallelism": f"dp{args.gpus} (independent batches per GPU, no collective)"}
+
+
+# ---------------------------------------------------------------------- companions
+
+def companions(ekv, torch, peaks):
+    """Gather (4 chunks of 8 prompts into a 4,096-page workspace) and demotion of 50% of
+    16,384 FP16 value pages, on the 32 x 8192-token gather/demote workload."""
+    from mixed_precision_paged_gb300 import roofline as rf
+    H, D, S = 8, 128, 16
+    P = 32 * 8192 // S
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1004)
+    k = torch.randn((P, S, H, D), generator=g, device="cuda").to(torch.float16)
+    vv = torch.randn((P, S, H, D), generator=g, device="cuda")
+    a = vv.abs().amax(dim=(1, 3))
+    sc = torch.where(a > 0, a / 448.0, torch.ones_like(a)).contiguous()
+    v8 = (vv / sc[:, None, :, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).reshape(P, -1)
+    del vv
+    bt = torch.randperm(P, generator=g, device="cuda").to(torch.int32).reshape(32, 512)
+    ws_k = torch.empty((4096, S, H, D), dtype=torch.float16, device="cuda")
+    ws_v = torch.empty_like(ws_k)
+    idx = torch.empty((4096,), dtype=torch.int32, device="cuda")
+    ctx = ekv.Context(H, H, D, 1)
+    chunks = [np.array([[s, 0, 512] for s in range(c * 8, c * 8 + 8)]) for c in range(4)]
+
+    def gather_all():
+        for pr in chunks:
+            ekv.ekv_gather_prefill(ctx.handle, k, v8, v8.shape[1], P, sc, 1, None, 1, bt, 512, 32, pr,
+                                   ws_k, ws_v, idx, 4096)
+    for _ in range(3):
+        gather_all()
+    torch.cuda.synchronize()
+    reps = 10
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        gather_all()
+    e.record()
+    torch.cuda.synchronize()
+    t_g = s.elapsed_time(e) / reps
+    gb = rf.gather_bytes(P, P, H, D, per_page_scales=True)
+    # demotion: FP16 pool N(0, 2), half of the pages
+    v16 = (torch.randn((P, S, H, D), generator=g, device="cuda") * math.sqrt(2.0)).to(torch.float16)
+    v16b = v16.view(torch.uint8).reshape(P, -1)
+    work = torch.empty_like(v16b)
+    mode = torch.zeros(P, dtype=torch.uint8, device="cuda")
+    scale_out = torch.zeros((P, H), dtype=torch.float32, device="cuda")
+    ids = torch.randperm(P, generator=g, device="cuda")[: P // 2].to(torch.int32)
+    ts = []
+    for rep in range(8):
+        work.copy_(v16b)
+        mode.zero_()
+        torch.cuda.synchronize()
+        s.record()
+        ekv.ekv_demote_pages(ctx.handle, work, work.shape[1], P, ids, P // 2, mode, scale_out)
+        e.record()
+        torch.cuda.synchronize()
+        if rep >= 3:
+            ts.append(s.elapsed_time(e))
+    t_d = float(np.median(ts))
+    db = rf.demote_bytes(P // 2, H, D)
+    err = ctx.error()
+    hbm = peaks["hbm_gbs"]
+    out = {"workload": "32 prompts x 8192 tokens (16,384 pages, 8 KV heads, D 128)",
+           "gather": {"ms": t_g, "GB/s": gb / t_g / 1e6, "frac_of_measured_hbm": gb / t_g / 1e6 / hbm,
+                      "bytes": gb, "what": "16,384 pages in 4 chunks of 4,096 into the FP16 workspace"},
+           "demote": {"ms": t_d, "GB/s": db / t_d / 1e6, "frac_of_measured_hbm": db / t_d / 1e6 / hbm,
+                      "bytes": db, "what": "8,192 of 16,384 FP16 value pages -> E4M3 + scales"},
+           "device_error": list(err)}
+    ctx.close()
+    return out
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ekv", choices=["ekv", "reference"])
+    ap.add_argument("--workload", default="pages_shape", choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
+    ap.add_argument("--variant", type=int, default=0, help="0 tensor-core, 1 CUDA-core consumer")
+    ap.add_argument("--seed", type=int, default=1002)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-companions", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from mixed_precision_paged_gb300 import build
+    if rank == 0:
+        build.ensure_built()
+    if world > 1:
+        dist.barrier()
+    from mixed_precision_paged_gb300 import ekv
+    from mixed_precision_paged_gb300 import roofline as rf
+    from mixed_precision_paged_gb300 import workloads as wl
+
+    wk = WORKLOADS[args.workload]
+    layers = args.layers or wk["layers"]
+    lens = lens_for(args.workload)
+    B, Hq, Hkv, D = len(lens), wk["q_heads"], wk["kv_heads"], wk["head_dim"]
+    cases = [wl.device_decode_case(lens, Hq, Hkv, D, v_format=wk["v_format"], scale_mode=wk["scale_mode"],
+                                   seed=args.seed + 7919 * (rank * 1000 + l)) for l in range(layers)]
+    torch.cuda.synchronize()
+    # algorithmic bytes per layer call
+    per_call = []
+    for c in cases:
+        if wk["v_format"] == "mixed":
+            modes = c.page_mode.cpu().numpy()
+            bt = c.block_table.cpu().numpy()
+            vbp = [[1 if modes[bt[b, j]] == 1 else 2 for j in range((l + 15) // 16)] for b, l in enumerate(lens)]
+            per_call.append(rf.decode_bytes(lens, Hq, Hkv, D, vbp, per_page_scales=True))
+        else:
+            per_call.append(rf.decode_bytes(lens, Hq, Hkv, D, 1 if wk["v_format"] == "e4m3" else 2,
+                                            per_page_scales=False))
+    step_bytes = sum(x["total"] for x in per_call)
+    split_bytes = float(np.mean([x["split"] for x in per_call]))
+
+    ctx = ekv.Context(Hq, Hkv, D, B, variant=args.variant)
+    outs = [torch.empty((B, Hq, D), dtype=torch.float16, device="cuda") for _ in range(layers)]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda") if layers == 1 else None
+
+    def step():
+        if flush is not None:
+            flush.zero_()
+        for l in range(layers):
+            ctx.decode(cases[l], outs[l], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ekv.ekv_profile_enable(ctx.handle, True)
+    ekv.ekv_profile_read(ctx.handle)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clock_rec = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if flush is not None:       # the flush writes are not decode work: time them alone
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            flush.zero_()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms -= f0.elapsed_time(f1)
+    split_ms, split_n = ekv.ekv_profile_read(ctx.handle)
+    ekv.ekv_profile_enable(ctx.handle, False)
+    err = ctx.error()
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end to end through the C ABI: per-step inputs from pinned host memory, outputs back
+    q_h = [c.q.cpu().pin_memory() for c in cases]
+    bt_h = [c.block_table.cpu().pin_memory() for c in cases]
+    sl_h = [c.seq_lens.cpu().pin_memory() for c in cases]
+    out_h = [torch.empty((B, Hq, D), dtype=torch.float16).pin_memory() for _ in range(layers)]
+    q_d = [torch.empty_like(c.q) for c in cases]
+    bt_d = [torch.empty_like(c.block_table) for c in cases]
+    sl_d = [torch.empty_like(c.seq_lens) for c in cases]
+    h2d = sum(q_h[l].numel() * 2 + bt_h[l].numel() * 4 + sl_h[l].numel() * 4 for l in range(layers))
+    d2h = sum(o.numel() * 2 for o in out_h)
+
+    def e2e_step():
+        for l in range(layers):
+            q_d[l].copy_(q_h[l], non_blocking=True)
+            bt_d[l].copy_(bt_h[l], non_blocking=True)
+            sl_d[l].copy_(sl_h[l], non_blocking=True)
+            c = cases[l]
+            ekv.ekv_paged_decode(ctx.handle, q_d[l], c.k_pages, c.v_pages, c.v_page_stride, c.num_pages,
+                                 c.v_scales, c.scale_mode, c.page_mode, c.uniform_mode, bt_d[l],
+                                 int(c.block_table.shape[1]), sl_d[l], B, 0.0, outs[l], None, stream)
+            out_h[l].copy_(outs[l], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    value = step_bytes * args.steps * world / (elapsed_ms / 1e3) / 1e9
+    e2e_value = step_bytes * args.e2e_steps * world / (e2e_ms / 1e3) / 1e9
+    ms_step = elapsed_ms / args.steps
+    achieved = split_bytes / (split_ms / split_n / 1e3) / 1e9 if split_n else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": config_of(args, wk),
+        "tokens_per_s": B * world / (ms_step / 1e3),
+        "hbm_frac_of_measured": value / world / hbm, "hbm_frac_of_8tbs_spec": value / world / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": (achieved / hbm) if achieved else None,
+                     "traffic": profiled_traffic(args.workload),
+                     "kernel": "decode_split_mma" if args.variant == 0 else "decode_split_simt",
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": split_bytes,
+                     "avg_launch_ms": split_ms / split_n if split_n else None},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps},
+        "gpu_launches": 2 * layers * args.steps,
+        "clocks": clock_rec,
+        "kv_dtype": "K f16, V e4m3 (compact) / f16 (TARGET); f32 accumulation",
+        "device_error": list(err),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cases, wk)
+    del cases
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_companions and args.workload == "pages_shape":
+        line["companions"] = companions(ekv, torch, peaks)
+    if rank == 0:
+        print(json.dumps(line))
+    ctx.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -20,11 +20,14 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + 1 TMA producer warp
 constexpr int kSmemBudget = 196608;                    // bytes of pipeline stages
 constexpr int kSplitSmemMax = 225280;                  // dynamic smem opt-in of the split kernels
 
-// plan buffer (int32): [0] per, [1] total, [2 .. 2+B] cu (page prefix sums),
-// [kPlanBad + b] bad flag of sequence b (set by the split kernel, cleared by merge).
-constexpr int kPlanCu = 2;
-constexpr int kPlanBad = kPlanCu + kMaxBatch + 1;
-constexpr int kPlanInts = kPlanBad + kMaxBatch;
+// plan buffer (int32), zeroed at context creation:
+//   [kPlanBad + b * 8 + h]    set when sequence b read bad data (page id, mode, scale,
+//                             length); the merge of (b, h) zeroes the output and clears it
+//   [kPlanTicket + b * 8 + h] partial records written so far for (b, KV head h); the
+//                             warp that brings it to its final count merges and resets it
+constexpr int kPlanBad = 0;
+constexpr int kPlanTicket = kPlanBad + kMaxBatch * kMaxKvHeads;
+constexpr int kPlanInts = kPlanTicket + kMaxBatch * kMaxKvHeads;
 
 struct DecodeParams {
   const __half* q;          // [B][Hq][D]
@@ -44,6 +47,7 @@ struct DecodeParams {
   int uniform_mode;
   int scale_mode;
   int Hq, Hkv, G, NG;       // NG = 8 / Hkv page groups per stage
+  int D;
   float qscale;             // sm_scale * log2(e)
 };
 
@@ -72,5 +76,6 @@ struct StageLayout {
 };
 
 cudaError_t set_smem_attr(const void* kern);
+size_t split_smem_bytes(int D, int vmode, int algo, int batch);
 
 }  // namespace ekv

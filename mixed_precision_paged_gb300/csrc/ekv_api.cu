@@ -17,7 +17,6 @@ cudaError_t launch_split_simt(const CUtensorMap& tk, const CUtensorMap& t8, cons
                               const DecodeParams& p, int D, int vmode, int grid, cudaStream_t st);
 cudaError_t launch_split_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
                              const DecodeParams& p, int D, int vmode, int grid, cudaStream_t st);
-cudaError_t launch_merge(const DecodeParams& p, int D, cudaStream_t st);
 }  // namespace ekv
 
 using namespace ekv;
@@ -230,6 +229,7 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
   p.NG = c->NG;
+  p.D = D;
   p.qscale = sm_scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -243,7 +243,6 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
     cudaEventRecord(c->ev[2 * c->ev_used + 1], st);
     ++c->ev_used;
   }
-  if (launch_merge(p, D, st) != cudaSuccess) return EKV_ERR_CUDA;
   return EKV_OK;
 }
 
@@ -353,6 +352,9 @@ ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {
   int h[4] = {0, 0, 0, 0};
   if (cudaMemcpy(h, c->err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return EKV_ERR_CUDA;
   if (cudaMemset(c->err, 0, sizeof(h)) != cudaSuccess) return EKV_ERR_CUDA;
+  // after a device error (a kernel may have wound down early) start the next call from
+  // a clean plan buffer: no stale tickets or flags
+  if (h[0] != 0 && cudaMemset(c->plan, 0, kPlanInts * sizeof(int)) != cudaSuccess) return EKV_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return EKV_ERR_CUDA;
   if (code) *code = h[0];
   if (detail) *detail = h[1];

@@ -117,9 +117,9 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
 // Per KV head h: a = max|x|, s = a / 448 (IEEE fp32 divide; 1 when a == 0),
 // code = E4M3_rn_satfinite(x / s). The whole FP16 page is loaded into registers
 // before the first barrier, so the codes may overwrite the page's first half.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 demote_kernel(const DemoteParams p) {
-  constexpr int kMaxVec = 16;                     // 16 x 16 B x 256 = 64 KiB (H_kv*D <= 2048)
+  constexpr int kMaxVec = 8;                      // 8 x 16 B x 256 = 32 KiB (H_kv*D <= 1024)
   __shared__ unsigned int s_amax[kMaxKvHeads];
   __shared__ float s_scale[kMaxKvHeads];
   __shared__ int s_nonfinite;
@@ -147,7 +147,7 @@ demote_kernel(const DemoteParams p) {
 #pragma unroll
   for (int u = 0; u < kMaxVec; ++u) {
     const int v = tid + u * 256;
-    if (u * 256 >= nvec) break;                   // warp-uniform: nvec is a multiple of 256
+    if (u * 256 >= nvec) break;                   // block-uniform
     unsigned int mx = 0u;
     if (v < nvec) {
       const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
