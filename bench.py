@@ -4,7 +4,7 @@ Default workload: asymmetric-KV decode at the pages' shape -- batch 32, context
 8192 + U{0..127}, 32 query / 8 KV heads, head dim 128, page size 16, NHD pages, K FP16,
 V FP8 E4M3 with a per-layer scale, 36 layers per step (36 distinct layer pools, 29 GB,
 so every layer call streams from HBM: inputs larger than L2, no flush needed).
-A step is one decode call per layer (split kernel + merge kernel each).
+A step is one decode call per layer (one kernel launch each: split work + fused merge).
 
 value        KV GB/s: algorithmic bytes of all layer calls / device time (CUDA events)
 e2e          the same metric through the C ABI with the per-step inputs (q, block
@@ -42,9 +42,9 @@ WORKLOADS = {
                              head_dim=128, layers=48, v_format="e4m3", scale_mode=0,
                              context="20% U[1,63], rest ceil(LogNormal(ln 2048, 1)) <= 32768"),
     "mixed": dict(desc="mixed-fidelity batch", batch=64, q_heads=32, kv_heads=8, head_dim=128,
-                  layers=1, v_format="mixed", scale_mode=1, context="U[512, 32768]"),
+                  layers=2, v_format="mixed", scale_mode=1, context="U[512, 32768]"),
     "mixed_fp16_control": dict(desc="mixed-fidelity batch, all-FP16 control", batch=64, q_heads=32,
-                               kv_heads=8, head_dim=128, layers=1, v_format="fp16", scale_mode=0,
+                               kv_heads=8, head_dim=128, layers=2, v_format="fp16", scale_mode=0,
                                context="U[512, 32768]"),
 }
 
@@ -305,7 +305,7 @@ def config_of(args, wk):
                           "fp16": "K fp16 / V fp16",
                           "mixed": "K fp16 / V per page fp16 or e4m3 (p=0.5), per-(page, head) scale"}[wk["v_format"]],
             "l2": "inputs larger than L2: distinct layer pools streamed in turn"
-                  if (args.layers or wk["layers"]) > 1 else "L2 flushed (1 GiB write) between steps",
+                  if (args.layers or wk["layers"]) > 1 else "L2 flushed (1 GiB read) between steps",
             "parallelism": f"dp{args.gpus} (independent batches per GPU, no collective)"}
 
 
@@ -442,11 +442,13 @@ def main():
     ctx = ekv.Context(Hq, Hkv, D, B, variant=args.variant)
     outs = [torch.empty((B, Hq, D), dtype=torch.float16, device="cuda") for _ in range(layers)]
     stream = torch.cuda.current_stream()
-    flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda") if layers == 1 else None
+    # one-layer runs evict L2 between steps by reading 1 GiB (a read leaves no dirty
+    # lines whose write-back would land inside the next timed decode)
+    flush = torch.ones(1 << 28, dtype=torch.int32, device="cuda") if layers == 1 else None
 
     def step():
         if flush is not None:
-            flush.zero_()
+            flush.sum()
         for l in range(layers):
             ctx.decode(cases[l], outs[l], stream=stream)
 
@@ -463,10 +465,12 @@ def main():
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("ekv_timed")
     t_start.record(stream)
     for _ in range(args.steps):
         step()
     t_end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -476,7 +480,7 @@ def main():
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(stream)
         for _ in range(args.steps):
-            flush.zero_()
+            flush.sum()
         f1.record(stream)
         torch.cuda.synchronize()
         elapsed_ms -= f0.elapsed_time(f1)
@@ -549,7 +553,7 @@ def main():
                      "avg_launch_ms": split_ms / split_n if split_n else None},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps},
-        "gpu_launches": 2 * layers * args.steps,
+        "gpu_launches": layers * args.steps,
         "clocks": clock_rec,
         "kv_dtype": "K f16, V e4m3 (compact) / f16 (TARGET); f32 accumulation",
         "device_error": list(err),

@@ -15,14 +15,14 @@ enum VMode { kVE4M3 = 0, kVFP16 = 1, kVMixed = 2 };
 // Consumer algorithm: CUDA-core FP32 FMAs or mma.sync tensor-core tiles.
 enum Algo { kAlgoSimt = 0, kAlgoMma = 1 };
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;   // + 1 TMA producer warp
-constexpr int kSmemBudget = 196608;                    // bytes of pipeline stages
-constexpr int kSplitSmemMax = 225280;                  // dynamic smem opt-in of the split kernels
+constexpr int kWarps = 8;                              // one warp per (KV head, page group)
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxSlots = 32;                          // ring slots per warp
+constexpr int kSplitSmemMax = 232448 - 1024;           // dynamic smem opt-in (static smem < 1 KB)
 
 // plan buffer (int32), zeroed at context creation:
-//   [kPlanBad + b * 8 + h]    set when sequence b read bad data (page id, mode, scale,
-//                             length); the merge of (b, h) zeroes the output and clears it
+//   [kPlanBad + b * 8 + h]    set when sequence b read bad data (page id, mode, scale);
+//                             the merge of (b, h) zeroes the output and clears it
 //   [kPlanTicket + b * 8 + h] partial records written so far for (b, KV head h); the
 //                             warp that brings it to its final count merges and resets it
 constexpr int kPlanBad = 0;
@@ -46,36 +46,28 @@ struct DecodeParams {
   int num_pages;
   int uniform_mode;
   int scale_mode;
-  int Hq, Hkv, G, NG;       // NG = 8 / Hkv page groups per stage
+  int Hq, Hkv, G, NG;       // NG = 8 / Hkv page groups (warps sharing a KV head)
   int D;
   float qscale;             // sm_scale * log2(e)
+  // shared-memory layout of the launch (set by the host for the slot size and batch)
+  int nsl;                  // ring slots per warp
+  int bar_off, cu_off, pbuf_off;
 };
 
-// Metadata of one page slot of a pipeline stage, written by the producer.
-struct PageMeta {
-  int page;
-  int ntok;     // valid tokens of this page (1..16)
-  int flags;    // kMetaCompact | kMetaSkip
-  int pad;
-  float scale[kMaxKvHeads];
-};
 constexpr int kMetaCompact = 1;
 constexpr int kMetaSkip = 2;
 
+// One ring slot holds one (page, KV head) slice: K [16][D] fp16 as D/64 TMA boxes of
+// 16 rows x 128 B, then V [16][D] as E4M3 rows (one box of 16 x D bytes) or fp16 (D/64
+// boxes). Slots are 1024-byte aligned, as the 128B swizzle requires.
 template <int D, int VMODE>
-struct StageLayout {
-  // One stage holds 8 (page, KV head) slices: NG = 8 / Hkv pages of Hkv heads.
-  static constexpr int kKStage = 8 * kPage * D * 2;                           // fp16 K
-  static constexpr int kVStage = 8 * kPage * D * (VMODE == kVE4M3 ? 1 : 2);   // V slot
-  static constexpr int kStageBytes = kKStage + kVStage;
-  static constexpr int kStages = kSmemBudget / kStageBytes;
-  static constexpr int kMetaOff = kStages * kStageBytes;
-  static constexpr int kBarOff = kMetaOff + kStages * 8 * (int)sizeof(PageMeta);
-  static constexpr int kCuOff = kBarOff + 2 * kStages * 8;
-  static_assert(kStages >= 2, "pipeline needs two stages");
+struct Slot {
+  static constexpr int kK = kPage * D * 2;
+  static constexpr int kV = kPage * D * (VMODE == kVE4M3 ? 1 : 2);
+  static constexpr int kBytes = kK + kV;
 };
 
 cudaError_t set_smem_attr(const void* kern);
-size_t split_smem_bytes(int D, int vmode, int algo, int batch);
+size_t split_layout(DecodeParams& p, int D, int vmode, int algo);
 
 }  // namespace ekv

@@ -79,20 +79,42 @@ __device__ __forceinline__ void e4m3_rows(uint32_t reg, uint32_t& row_d, uint32_
 }
 
 template <int D, int VMODE>
-__device__ void consume_mma(const DecodeParams& p, uint8_t* stages, PageMeta* meta, uint64_t* full,
-                            uint64_t* empty, const int* cu, int start, int end, int b_first, int b_last, int per) {
-  using L = StageLayout<D, VMODE>;
+__device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV8,
+                            const CUtensorMap* tmV16, uint8_t* smem, int start, int end, int b_first,
+                            int b_last, int per) {
+  using S = Slot<D, VMODE>;
   constexpr int KS = D / 16;   // k-steps of QK
   constexpr int MT = D / 16;   // m-tiles of PV
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = p.Hkv, NG = p.NG, G = p.G;
   const int h = warp % Hkv, grp = warp / Hkv;
   const int q4 = lane & 3, r8 = lane >> 2;          // fragment coordinates
-  const int k_sub = L::kKStage / NG, v_sub = L::kVStage / NG;
   const bool uniform_scale = VMODE == kVE4M3 && p.scale_mode == EKV_SCALE_PER_TENSOR;
   // ldmatrix row address pattern (token, 16-byte chunk offset) of this lane
   const int lm_t = (lane & 7) + ((lane >> 3) & 1) * 8;
   const int lm_c = lane >> 4;
+  const int* cu = reinterpret_cast<const int*>(smem + p.cu_off);
+  const WarpRing ring = warp_ring(p, smem, S::kBytes);
+  const int n_range = end - start;
+  const int n_my = n_range > grp ? (n_range - grp + NG - 1) / NG : 0;   // this warp's pages
+
+  // metadata of the warp's pages, 32 per batch, one per lane: cur = batch of k,
+  // nxt = next batch (mode bytes / scales in flight), nxt2 = the one after (ids in flight)
+  const float tensor_scale =
+      (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR) ? __ldg(p.v_scales) : 1.f;
+  WarpMeta cur, nxt, nxt2;
+  wm_ids(p, cu, start, n_my, grp, lane, cur);
+  wm_ids(p, cu, start, n_my, grp, 32 + lane, nxt);
+  wm_meta<VMODE>(p, tensor_scale, h, cur);
+  {
+    const int n0 = min(ring.nsl, n_my);              // prime the ring
+    for (int kk = 0; kk < n0; ++kk)
+      ring_issue<D, VMODE>(ring, kk, h, __shfl_sync(0xffffffffu, cur.page, kk),
+                           __shfl_sync(0xffffffffu, cur.flags, kk), tmK, tmV8, tmV16);
+  }
+  wm_meta<VMODE>(p, tensor_scale, h, nxt);
+  wm_ids(p, cu, start, n_my, grp, 64 + lane, nxt2);
+  int k = 0;                                        // next page of this warp
 
   for (int b = b_first; b <= b_last; ++b) {
     const int j0 = max(cu[b], start), j1 = min(cu[b + 1], end);
@@ -113,37 +135,43 @@ __device__ void consume_mma(const DecodeParams& p, uint8_t* stages, PageMeta* me
     for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY;           // running max of g = 2q4, 2q4 + 1
     float l0 = 0.f, l1 = 0.f;                       // this lane's share of the sums
-    const int r_begin = j0 - start, r_end = j1 - start;
-    int r = r_begin + (((grp - r_begin) % NG) + NG) % NG;
-    for (; r < r_end; r += NG) {
-      const int si = r / NG;
-      const int stage = si % L::kStages;
-      const uint32_t ph = (uint32_t)(si / L::kStages) & 1u;
-      if (!mbar_wait(&full[stage], ph)) {
+    const int r_end = j1 - start;
+    for (; k < n_my && grp + k * NG < r_end; ++k) {
+      if ((k & 31) == 0 && k > 0) {                 // next metadata batch
+        cur = nxt;
+        nxt = nxt2;
+        wm_meta<VMODE>(p, tensor_scale, h, nxt);
+        wm_ids(p, cu, start, n_my, grp, k + 64 + lane, nxt2);
+      }
+      const int s_idx = k % ring.nsl;
+      if (!mbar_wait(&ring.full[s_idx], (uint32_t)(k / ring.nsl) & 1u)) {
         if (lane == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_TIMEOUT, blockIdx.x);
+        // drain this warp's other fills in flight (bounded), then stop
+        for (int kk = k + 1; kk < min(k + ring.nsl, n_my); ++kk)
+          mbar_wait(&ring.full[kk % ring.nsl], (uint32_t)(kk / ring.nsl) & 1u);
         return;
       }
-      const PageMeta& mt = meta[stage * 8 + grp];
-      const int flags = mt.flags;
-      const int ntok = mt.ntok;
+      const int flags = __shfl_sync(0xffffffffu, cur.flags, k & 31);
+      const int ntok = __shfl_sync(0xffffffffu, cur.ntok, k & 31);
+      const float pscale = __shfl_sync(0xffffffffu, cur.scale, k & 31);
       const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (flags & kMetaCompact));
       const bool skip = (flags & kMetaSkip) != 0;
-      const float vs = (compact && !uniform_scale) ? mt.scale[h] : 1.f;
-      // Pull this (page, head) slice into registers and free the stage at once, so
-      // that the producer can refill it while the tiles are multiplied: K as QK A
+      const float vs = (compact && !uniform_scale) ? pscale : 1.f;
+      // Pull this (page, head) slice into registers and refill its slot at once, so
+      // that the next fill is in flight while the tiles are multiplied: K as QK A
       // fragments, V as raw rows (E4M3: ldmatrix.trans byte pairs; FP16: 32-bit words).
       uint32_t kf[KS][4];
       uint32_t vr[MT][4];
       if (!skip) {
-        const uint32_t kp = smem_u32(stages + stage * L::kStageBytes + grp * k_sub);
-        const uint32_t vp = smem_u32(stages + stage * L::kStageBytes + L::kKStage + grp * v_sub);
+        const uint32_t kp = smem_u32(ring.slots + (size_t)s_idx * S::kBytes);
+        const uint32_t vp = kp + S::kK;
 #pragma unroll
         for (int s = 0; s < KS; ++s) {
           const int kb = s >> 2, c = 2 * (s & 3) + lm_c;
-          ldsm_x4(kp + (kb * Hkv + h) * 2048 + swz128(lm_t * 128 + c * 16), kf[s][0], kf[s][1], kf[s][2], kf[s][3]);
+          ldsm_x4(kp + kb * 2048 + swz128(lm_t * 128 + c * 16), kf[s][0], kf[s][1], kf[s][2], kf[s][3]);
         }
         if (compact) {
-          const uint32_t vbox = vp + h * (kPage * D);
+          const uint32_t vbox = vp;
 #pragma unroll
           for (int j = 0; j < MT / 2; ++j) {
             const int c = 2 * j + lm_c;
@@ -154,7 +182,7 @@ __device__ void consume_mma(const DecodeParams& p, uint8_t* stages, PageMeta* me
 #pragma unroll
           for (int i = 0; i < MT; ++i) {
             const int d = 16 * i + 2 * r8;
-            const uint32_t box = vp + ((d >> 6) * Hkv + h) * 2048;
+            const uint32_t box = vp + (d >> 6) * 2048;
             const uint32_t col = (d & 63) * 2;
             const int t0 = 2 * q4;
             vr[i][0] = lds_u32(box + swz128(t0 * 128 + col));
@@ -164,8 +192,18 @@ __device__ void consume_mma(const DecodeParams& p, uint8_t* stages, PageMeta* me
           }
         }
       }
+      // the slice is in registers: refill the slot with this warp's page k + nsl
+      fence_reads_before_refill();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      {
+        const int kk = k + ring.nsl;
+        if (kk < n_my) {
+          const bool in_cur = (kk >> 5) == (k >> 5);
+          const int pg = __shfl_sync(0xffffffffu, in_cur ? cur.page : nxt.page, kk & 31);
+          const int fl = __shfl_sync(0xffffffffu, in_cur ? cur.flags : nxt.flags, kk & 31);
+          ring_issue<D, VMODE>(ring, kk, h, pg, fl, tmK, tmV8, tmV16);
+        }
+      }
       if (!skip) {
         // ---- QK on the tensor cores: two independent accumulation chains
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -281,61 +319,39 @@ template <int D, int VMODE>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_split_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV8,
                  const __grid_constant__ CUtensorMap tmV16, const DecodeParams p) {
-  using L = StageLayout<D, VMODE>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int warp_tot[kThreads / 32];
-  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  uint8_t* smem = smem_raw + pad;
-  uint8_t* stages = smem;
-  PageMeta* meta = reinterpret_cast<PageMeta*>(smem + L::kMetaOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + L::kStages;
-  int* cu = reinterpret_cast<int*>(smem + L::kCuOff);
-
-  const int total = plan_pages(p, cu, warp_tot);
-  const int per = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 1;
-  if (blockIdx.x == 0) write_empty_sequences(p);
-  const int start = (int)blockIdx.x * per;
-  const int end = min(total, start + per);
-  if (start >= end) return;
+  uint8_t* smem = aligned_smem(smem_raw);
+  int start, end, per, b_first, b_last;
+  if (!split_prologue(p, smem, warp_tot, start, end, per, b_first, b_last)) return;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(&full[s], (uint32_t)p.NG);
-      mbar_init(&empty[s], (uint32_t)kConsumerWarps);
-    }
-    fence_barrier_init();
+    tma_prefetch_desc(&tmK);
+    if (VMODE != kVFP16) tma_prefetch_desc(&tmV8);
+    if (VMODE != kVE4M3) tma_prefetch_desc(&tmV16);
   }
-  __syncthreads();
-  const int b_first = upper_bound_i(cu, p.batch + 1, start) - 1;
-  const int b_last = upper_bound_i(cu, p.batch + 1, end - 1) - 1;
-  if ((threadIdx.x >> 5) == kConsumerWarps) {
-    produce<D, VMODE>(p, &tmK, &tmV8, &tmV16, stages, meta, full, empty, cu, start, end);
-  } else {
-    consume_mma<D, VMODE>(p, stages, meta, full, empty, cu, start, end, b_first, b_last, per);
-  }
+  consume_mma<D, VMODE>(p, &tmK, &tmV8, &tmV16, smem, start, end, b_first, b_last, per);
 }
 
 template <int D, int VMODE>
 static cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
-                              const DecodeParams& p, int grid, cudaStream_t st) {
+                              const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
   auto kern = decode_split_mma<D, VMODE>;
   cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
-  const size_t smem = split_smem_bytes(D, VMODE, kAlgoMma, p.batch);
   kern<<<grid, kThreads, smem, st>>>(tk, t8, t16, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_split_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
-                             const DecodeParams& p, int D, int vmode, int grid, cudaStream_t st) {
+                             const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st) {
   if (D == 128) {
-    if (vmode == kVE4M3) return launch_mma<128, kVE4M3>(tk, t8, t16, p, grid, st);
-    if (vmode == kVFP16) return launch_mma<128, kVFP16>(tk, t8, t16, p, grid, st);
-    return launch_mma<128, kVMixed>(tk, t8, t16, p, grid, st);
+    if (vmode == kVE4M3) return launch_mma<128, kVE4M3>(tk, t8, t16, p, grid, smem, st);
+    if (vmode == kVFP16) return launch_mma<128, kVFP16>(tk, t8, t16, p, grid, smem, st);
+    return launch_mma<128, kVMixed>(tk, t8, t16, p, grid, smem, st);
   }
-  if (vmode == kVE4M3) return launch_mma<64, kVE4M3>(tk, t8, t16, p, grid, st);
-  if (vmode == kVFP16) return launch_mma<64, kVFP16>(tk, t8, t16, p, grid, st);
-  return launch_mma<64, kVMixed>(tk, t8, t16, p, grid, st);
+  if (vmode == kVE4M3) return launch_mma<64, kVE4M3>(tk, t8, t16, p, grid, smem, st);
+  if (vmode == kVFP16) return launch_mma<64, kVFP16>(tk, t8, t16, p, grid, smem, st);
+  return launch_mma<64, kVMixed>(tk, t8, t16, p, grid, smem, st);
 }
 
 }  // namespace ekv

@@ -18,10 +18,10 @@ namespace ekv {
 // block of tokens tg, tg+4, tg+8, tg+12 (8 lanes share a token and reduce with three
 // xor shuffles). For PV every lane owns D/32 consecutive columns of every token.
 template <int D, int GP, int VMODE>
-__device__ void consume_simt(const DecodeParams& p, uint8_t* stages, PageMeta* meta,
-                             uint64_t* full, uint64_t* empty, const int* cu, int start,
-                             int end, int b_first, int b_last, int per, float* pbuf_all) {
-  using L = StageLayout<D, VMODE>;
+__device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV8,
+                             const CUtensorMap* tmV16, uint8_t* smem, int start, int end, int b_first,
+                             int b_last, int per) {
+  using S = Slot<D, VMODE>;
   constexpr int DPL = D / 8;
   constexpr int VPL = D / 32;
   constexpr int KB = D / 64;
@@ -29,8 +29,23 @@ __device__ void consume_simt(const DecodeParams& p, uint8_t* stages, PageMeta* m
   const int Hkv = p.Hkv, NG = p.NG, G = p.G;
   const int h = warp % Hkv, grp = warp / Hkv;
   const int tg = lane >> 3, c8 = lane & 7;
-  float* pbuf = pbuf_all + warp * (kPage * GP);
-  const int k_sub = L::kKStage / NG, v_sub = L::kVStage / NG;
+  float* pbuf = reinterpret_cast<float*>(smem + p.pbuf_off) + warp * (kPage * GP);
+  const int* cu = reinterpret_cast<const int*>(smem + p.cu_off);
+  const WarpRing ring = warp_ring(p, smem, S::kBytes);
+  const int n_range = end - start;
+  const int n_my = n_range > grp ? (n_range - grp + NG - 1) / NG : 0;
+  const float tensor_scale =
+      (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR) ? __ldg(p.v_scales) : 1.f;
+  WarpMeta cur, nxt, nxt2;
+  wm_ids(p, cu, start, n_my, grp, lane, cur);
+  wm_ids(p, cu, start, n_my, grp, 32 + lane, nxt);
+  wm_meta<VMODE>(p, tensor_scale, h, cur);
+  for (int kk = 0; kk < min(ring.nsl, n_my); ++kk)
+    ring_issue<D, VMODE>(ring, kk, h, __shfl_sync(0xffffffffu, cur.page, kk),
+                         __shfl_sync(0xffffffffu, cur.flags, kk), tmK, tmV8, tmV16);
+  wm_meta<VMODE>(p, tensor_scale, h, nxt);
+  wm_ids(p, cu, start, n_my, grp, 64 + lane, nxt2);
+  int k = 0;
 
   for (int b = b_first; b <= b_last; ++b) {
     const int j0 = max(cu[b], start), j1 = min(cu[b + 1], end);
@@ -61,23 +76,30 @@ __device__ void consume_simt(const DecodeParams& p, uint8_t* stages, PageMeta* m
 #pragma unroll
       for (int x = 0; x < VPL; ++x) acc[g][x] = 0.f;
     }
-    const int r_begin = j0 - start, r_end = j1 - start;
-    int r = r_begin + (((grp - r_begin) % NG) + NG) % NG;
-    for (; r < r_end; r += NG) {
-      const int si = r / NG;
-      const int stage = si % L::kStages;
-      const uint32_t ph = (uint32_t)(si / L::kStages) & 1u;
-      if (!mbar_wait(&full[stage], ph)) {
+    const int r_end = j1 - start;
+    for (; k < n_my && grp + k * NG < r_end; ++k) {
+      if ((k & 31) == 0 && k > 0) {
+        cur = nxt;
+        nxt = nxt2;
+        wm_meta<VMODE>(p, tensor_scale, h, nxt);
+        wm_ids(p, cu, start, n_my, grp, k + 64 + lane, nxt2);
+      }
+      const int s_idx = k % ring.nsl;
+      if (!mbar_wait(&ring.full[s_idx], (uint32_t)(k / ring.nsl) & 1u)) {
         if (lane == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_TIMEOUT, blockIdx.x);
+        for (int kk = k + 1; kk < min(k + ring.nsl, n_my); ++kk)
+          mbar_wait(&ring.full[kk % ring.nsl], (uint32_t)(kk / ring.nsl) & 1u);
         return;
       }
-      const PageMeta& mt = meta[stage * 8 + grp];
-      if (!(mt.flags & kMetaSkip)) {
-        const uint8_t* kp = stages + stage * L::kStageBytes + grp * k_sub;
-        const uint8_t* vp = stages + stage * L::kStageBytes + L::kKStage + grp * v_sub;
-        const int ntok = mt.ntok;
-        const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (mt.flags & kMetaCompact));
-        const float vs = compact ? mt.scale[h] : 1.f;
+      const int mflags = __shfl_sync(0xffffffffu, cur.flags, k & 31);
+      const int mntok = __shfl_sync(0xffffffffu, cur.ntok, k & 31);
+      const float mscale = __shfl_sync(0xffffffffu, cur.scale, k & 31);
+      if (!(mflags & kMetaSkip)) {
+        const uint8_t* kp = ring.slots + (size_t)s_idx * S::kBytes;
+        const uint8_t* vp = kp + S::kK;
+        const int ntok = mntok;
+        const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (mflags & kMetaCompact));
+        const float vs = compact ? mscale : 1.f;
         float s[4][GP];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -86,7 +108,7 @@ __device__ void consume_simt(const DecodeParams& p, uint8_t* stages, PageMeta* m
 #pragma unroll
           for (int kb = 0; kb < KB; ++kb) {
             const uint4 raw = *reinterpret_cast<const uint4*>(
-                kp + (kb * Hkv + h) * 2048 + swz128(t * 128 + c8 * 16));
+                kp + kb * 2048 + swz128(t * 128 + c8 * 16));
             const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -131,13 +153,13 @@ __device__ void consume_simt(const DecodeParams& p, uint8_t* stages, PageMeta* m
           if (compact) {
             if (D == 128) {
               const uint32_t w4 = *reinterpret_cast<const uint32_t*>(
-                  vp + h * (kPage * D) + swz128(t * 128 + lane * 4));
+                  vp + swz128(t * 128 + lane * 4));
               const float2 a = e4m3x2_to_float2((uint16_t)(w4 & 0xffffu));
               const float2 c = e4m3x2_to_float2((uint16_t)(w4 >> 16));
               vv[0] = a.x; vv[1] = a.y; vv[2 % VPL] = c.x; vv[3 % VPL] = c.y;
             } else {
               const uint16_t w2 = *reinterpret_cast<const uint16_t*>(
-                  vp + h * (kPage * D) + swz64(t * 64 + lane * 2));
+                  vp + swz64(t * 64 + lane * 2));
               const float2 a = e4m3x2_to_float2(w2);
               vv[0] = a.x; vv[1 % VPL] = a.y;
             }
@@ -145,13 +167,13 @@ __device__ void consume_simt(const DecodeParams& p, uint8_t* stages, PageMeta* m
             if (D == 128) {
               const int kb = lane >> 4;
               const uint2 w = *reinterpret_cast<const uint2*>(
-                  vp + (kb * Hkv + h) * 2048 + swz128(t * 128 + (lane & 15) * 8));
+                  vp + kb * 2048 + swz128(t * 128 + (lane & 15) * 8));
               const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
               const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
               vv[0] = a.x; vv[1] = a.y; vv[2 % VPL] = c.x; vv[3 % VPL] = c.y;
             } else {
               const uint32_t w = *reinterpret_cast<const uint32_t*>(
-                  vp + h * 2048 + swz128(t * 128 + lane * 4));
+                  vp + swz128(t * 128 + lane * 4));
               const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w));
               vv[0] = a.x; vv[1 % VPL] = a.y;
             }
@@ -166,8 +188,16 @@ __device__ void consume_simt(const DecodeParams& p, uint8_t* stages, PageMeta* m
         }
         __syncwarp();
       }
+      // this consumer reads the slot while it computes: refill it afterwards
+      fence_reads_before_refill();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      const int kk = k + ring.nsl;
+      if (kk < n_my) {
+        const bool in_cur = (kk >> 5) == (k >> 5);
+        const int pg = __shfl_sync(0xffffffffu, in_cur ? cur.page : nxt.page, kk & 31);
+        const int fl = __shfl_sync(0xffffffffu, in_cur ? cur.flags : nxt.flags, kk & 31);
+        ring_issue<D, VMODE>(ring, kk, h, pg, fl, tmK, tmV8, tmV16);
+      }
     }
     // partial record of (segment b, this CTA, page group grp) for this KV head's G heads
     const size_t R = (size_t)(b + blockIdx.x) * NG + grp;
@@ -194,39 +224,12 @@ template <int D, int GP, int VMODE>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_split_simt(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV8,
                   const __grid_constant__ CUtensorMap tmV16, const DecodeParams p) {
-  using L = StageLayout<D, VMODE>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int warp_tot[kThreads / 32];
-  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  uint8_t* smem = smem_raw + pad;
-  uint8_t* stages = smem;
-  PageMeta* meta = reinterpret_cast<PageMeta*>(smem + L::kMetaOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + L::kStages;
-  int* cu = reinterpret_cast<int*>(smem + L::kCuOff);
-  float* pbuf = reinterpret_cast<float*>(smem + L::kCuOff + (((p.batch + 1) * 4 + 15) & ~15));
-
-  const int total = plan_pages(p, cu, warp_tot);
-  const int per = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 1;
-  if (blockIdx.x == 0) write_empty_sequences(p);
-  const int start = (int)blockIdx.x * per;
-  const int end = min(total, start + per);
-  if (start >= end) return;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(&full[s], (uint32_t)p.NG);
-      mbar_init(&empty[s], (uint32_t)kConsumerWarps);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-  const int b_first = upper_bound_i(cu, p.batch + 1, start) - 1;
-  const int b_last = upper_bound_i(cu, p.batch + 1, end - 1) - 1;
-  if ((threadIdx.x >> 5) == kConsumerWarps) {
-    produce<D, VMODE>(p, &tmK, &tmV8, &tmV16, stages, meta, full, empty, cu, start, end);
-  } else {
-    consume_simt<D, GP, VMODE>(p, stages, meta, full, empty, cu, start, end, b_first, b_last, per, pbuf);
-  }
+  uint8_t* smem = aligned_smem(smem_raw);
+  int start, end, per, b_first, b_last;
+  if (!split_prologue(p, smem, warp_tot, start, end, per, b_first, b_last)) return;
+  consume_simt<D, GP, VMODE>(p, &tmK, &tmV8, &tmV16, smem, start, end, b_first, b_last, per);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -263,23 +266,37 @@ static cudaError_t dispatch_simt_g(const CUtensorMap& tk, const CUtensorMap& t8,
   return launch_simt<D, 8, VMODE>(tk, t8, t16, p, grid, smem, st);
 }
 
-size_t split_smem_bytes(int D, int vmode, int algo, int batch) {
-  int cu_off = 0;
+// Shared-memory layout of a split launch: 8 rings of as many slots as fit next to the
+// barriers, the page prefix sums of `batch` sequences and (CUDA-core consumer) the
+// probability buffer. Returns the dynamic smem bytes to request.
+template <int D, int VMODE>
+static size_t layout_for(DecodeParams& p, int algo) {
+  using S = Slot<D, VMODE>;
+  const size_t cu_bytes = ((size_t)(p.batch + 1) * 4 + 15) & ~(size_t)15;
+  const size_t pbuf_bytes = algo == kAlgoSimt ? (size_t)kWarps * kPage * 8 * 4 : 0;
+  const size_t fixed = 1024 + cu_bytes + pbuf_bytes;
+  int nsl = (int)((kSplitSmemMax - fixed) / ((size_t)kWarps * (S::kBytes + 8)));
+  nsl = nsl > kMaxSlots ? kMaxSlots : nsl;
+  p.nsl = nsl;
+  p.bar_off = kWarps * nsl * S::kBytes;
+  p.cu_off = p.bar_off + kWarps * nsl * 8;
+  p.pbuf_off = p.cu_off + (int)cu_bytes;
+  return 1024 + (size_t)p.pbuf_off + pbuf_bytes;
+}
+
+size_t split_layout(DecodeParams& p, int D, int vmode, int algo) {
   if (D == 128) {
-    cu_off = vmode == kVE4M3 ? StageLayout<128, kVE4M3>::kCuOff
-           : vmode == kVFP16 ? StageLayout<128, kVFP16>::kCuOff : StageLayout<128, kVMixed>::kCuOff;
-  } else {
-    cu_off = vmode == kVE4M3 ? StageLayout<64, kVE4M3>::kCuOff
-           : vmode == kVFP16 ? StageLayout<64, kVFP16>::kCuOff : StageLayout<64, kVMixed>::kCuOff;
+    if (vmode == kVE4M3) return layout_for<128, kVE4M3>(p, algo);
+    if (vmode == kVFP16) return layout_for<128, kVFP16>(p, algo);
+    return layout_for<128, kVMixed>(p, algo);
   }
-  size_t bytes = 1024 + (size_t)cu_off + (((size_t)(batch + 1) * 4 + 15) & ~(size_t)15);
-  if (algo == kAlgoSimt) bytes += (size_t)kConsumerWarps * kPage * 8 * 4;
-  return bytes;
+  if (vmode == kVE4M3) return layout_for<64, kVE4M3>(p, algo);
+  if (vmode == kVFP16) return layout_for<64, kVFP16>(p, algo);
+  return layout_for<64, kVMixed>(p, algo);
 }
 
 cudaError_t launch_split_simt(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
-                              const DecodeParams& p, int D, int vmode, int grid, cudaStream_t st) {
-  const size_t smem = split_smem_bytes(D, vmode, kAlgoSimt, p.batch);
+                              const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st) {
   if (D == 128) {
     if (vmode == kVE4M3) return dispatch_simt_g<128, kVE4M3>(tk, t8, t16, p, grid, smem, st);
     if (vmode == kVFP16) return dispatch_simt_g<128, kVFP16>(tk, t8, t16, p, grid, smem, st);

@@ -12,11 +12,10 @@
 #include "gather_demote.cuh"
 
 namespace ekv {
-size_t split_smem_bytes(int D, int vmode, int algo, int batch);
 cudaError_t launch_split_simt(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
-                              const DecodeParams& p, int D, int vmode, int grid, cudaStream_t st);
+                              const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_split_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
-                             const DecodeParams& p, int D, int vmode, int grid, cudaStream_t st);
+                             const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st);
 }  // namespace ekv
 
 using namespace ekv;
@@ -124,13 +123,13 @@ ekv_status ekv_create(ekv_ctx** out, const ekv_config* cfg) {
   ekv_ctx* c = new (std::nothrow) ekv_ctx();
   if (!c) return EKV_ERR_CUDA;
   c->cfg = *cfg;
-  c->NG = kConsumerWarps / cfg->num_kv_heads;
+  c->NG = kWarps / cfg->num_kv_heads;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
     delete c;
     return EKV_ERR_CUDA;
   }
-  c->split_ctas = c->num_sms;                     // one 288-thread CTA per SM (~200 KB smem)
+  c->split_ctas = c->num_sms;                     // one 256-thread CTA per SM (~220 KB smem)
   const size_t records = (size_t)(cfg->max_batch + c->split_ctas) * c->NG;
   const size_t hq = (size_t)cfg->num_q_heads;
   bool ok = cudaMalloc(&c->part_acc, records * hq * cfg->head_dim * sizeof(float)) == cudaSuccess &&
@@ -236,8 +235,10 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
   c->last_stream = st;
   const bool timed = c->profiling && c->ev_used * 2 + 1 < c->ev.size();
   if (timed) cudaEventRecord(c->ev[2 * c->ev_used], st);
-  cudaError_t e = c->variant == 1 ? launch_split_simt(tk, t8, t16, p, D, vmode, c->split_ctas, st)
-                                  : launch_split_mma(tk, t8, t16, p, D, vmode, c->split_ctas, st);
+  const int algo = c->variant == 1 ? kAlgoSimt : kAlgoMma;
+  const size_t smem = split_layout(p, D, vmode, algo);
+  cudaError_t e = algo == kAlgoSimt ? launch_split_simt(tk, t8, t16, p, D, vmode, c->split_ctas, smem, st)
+                                    : launch_split_mma(tk, t8, t16, p, D, vmode, c->split_ctas, smem, st);
   if (e != cudaSuccess) return EKV_ERR_CUDA;
   if (timed) {
     cudaEventRecord(c->ev[2 * c->ev_used + 1], st);

@@ -1,5 +1,6 @@
-// pipeline.cuh -- the parts of the split-K decode that every consumer shares: the
-// device-side plan (page prefix sum over seq_lens) and the TMA producer warp.
+// pipeline.cuh -- the parts of the split-K decode that both consumers share: the
+// device-side plan (page prefix sum over seq_lens), the per-warp TMA rings, the
+// per-warp metadata prefetch and the fused split merge.
 //
 // Work split: the pages of all sequences form one stream (cu = page prefix sum,
 // computed by every CTA from seq_lens); CTA c takes pages [c*per, (c+1)*per) of it,
@@ -10,12 +11,12 @@
 // cu[b]/per .. (cu[b+1]-1)/per and those ranges of consecutive sequences only meet
 // at one CTA.
 //
-// Pipeline: warp 8 is the producer. For each page it reads the block-table entry,
-// the mode byte and the scales (32 pages at a time, one per lane), and issues one TMA
-// box per (KV head, 64-element column block) of K and V into a stage; the boxes land
-// 128B/64B-swizzled so that the consumers' 16-byte row reads are bank-conflict free.
-// A stage holds 8 (page, KV head) slices: NG = 8 / H_kv consecutive pages. Consumer
-// warp w handles KV head w % H_kv of the stage's page w / H_kv.
+// Rings: warp w owns KV head h = w % Hkv and page group grp = w / Hkv (NG = 8 / Hkv
+// groups): it handles the slices (page r, head h) of the CTA's pages r = grp, grp + NG,
+// ... in order. Each warp keeps its own ring of `nsl` slots in shared memory and feeds
+// it itself: one TMA box per 64-column block of K and of V, 128B/64B-swizzled so that
+// the warp's 16-byte row reads are bank-conflict free. No warp waits for another, and a
+// slot is refilled as soon as its owner has pulled the slice into registers.
 #pragma once
 
 #include "decode.cuh"
@@ -36,12 +37,12 @@ __device__ __forceinline__ void mark_bad(const DecodeParams& p, int b) {
 }
 
 // Sequences with no pages (length 0, or a length the block table cannot hold) are
-// touched by no CTA: CTA 0 writes their zero output and -inf lse.
-__device__ __forceinline__ void write_empty_sequences(const DecodeParams& p) {
+// touched by no CTA: CTA 0 writes their zero output and -inf lse, reading the page
+// prefix sums already in shared memory (no global loads on this path).
+__device__ __forceinline__ void write_empty_sequences(const DecodeParams& p, const int* cu) {
   const int n = p.Hq * p.D;
   for (int b = 0; b < p.batch; ++b) {
-    const int L = __ldg(p.seq_lens + b);
-    if (L > 0 && L <= p.bt_stride * kPage) continue;
+    if (cu[b + 1] != cu[b]) continue;
     for (int i = threadIdx.x; i < n; i += blockDim.x) p.out[(size_t)b * n + i] = __float2half(0.f);
     if (p.lse)
       for (int i = threadIdx.x; i < p.Hq; i += blockDim.x) p.lse[(size_t)b * p.Hq + i] = -INFINITY;
@@ -53,7 +54,7 @@ __device__ __forceinline__ void write_empty_sequences(const DecodeParams& p) {
 // (by CTA 0 only) and flagged so that the merge zeroes them.
 __device__ __forceinline__ int plan_pages(const DecodeParams& p, int* cu, int* warp_tot) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int kWarps = kThreads / 32;
+  constexpr int kNW = kThreads / 32;
   if (tid == 0) cu[0] = 0;
   int carry = 0;
   for (int base = 0; base < p.batch; base += kThreads) {
@@ -77,7 +78,7 @@ __device__ __forceinline__ int plan_pages(const DecodeParams& p, int* cu, int* w
     __syncthreads();
     int woff = 0, chunk = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kNW; ++w) {
       const int t = warp_tot[w];
       woff += (w < warp) ? t : 0;
       chunk += t;
@@ -89,25 +90,26 @@ __device__ __forceinline__ int plan_pages(const DecodeParams& p, int* cu, int* w
   return carry;
 }
 
-// ------------------------------------------------------------------------ producer
-// Metadata of the page slot r of this CTA's range, one lane per slot.
-struct SlotMeta {
+// ----------------------------------------------------------- per-warp metadata
+// Metadata of the warp's k-th page, one page per lane for 32 consecutive k.
+struct WarpMeta {
   int page;
   int ntok;
   int flags;
   int b;
-  float sc[kMaxKvHeads];
+  float scale;
 };
 
-// Stage A: block-table entry of slot r (the load is consumed one batch later).
-__device__ __forceinline__ void slot_ids(const DecodeParams& p, const int* cu, int start, int n_range, int r,
-                                         SlotMeta& m) {
+// Stage A: block-table entry of the warp's page k (consumed a batch later).
+__device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int start, int n_my, int grp, int k,
+                                       WarpMeta& m) {
   m.page = 0;
   m.ntok = 0;
   m.flags = kMetaSkip;
   m.b = -1;
-  if (r < n_range) {
-    const int j = start + r;
+  m.scale = 1.f;
+  if (k < n_my) {
+    const int j = start + grp + k * p.NG;
     const int b = upper_bound_i(cu, p.batch + 1, j) - 1;
     const int lp = j - cu[b];
     m.b = b;
@@ -117,11 +119,9 @@ __device__ __forceinline__ void slot_ids(const DecodeParams& p, const int* cu, i
   }
 }
 
-// Stage B: checks, mode byte and scales of a slot whose page id is known.
+// Stage B: checks, mode byte and the KV head's scale of a page whose id is known.
 template <int VMODE>
-__device__ __forceinline__ void slot_meta(const DecodeParams& p, float tensor_scale, SlotMeta& m) {
-#pragma unroll
-  for (int h = 0; h < kMaxKvHeads; ++h) m.sc[h] = 1.f;
+__device__ __forceinline__ void wm_meta(const DecodeParams& p, float tensor_scale, int h, WarpMeta& m) {
   if (m.b < 0) return;
   const int b = m.b, page = m.page;
   if (page < 0 || page >= p.num_pages) {
@@ -138,22 +138,11 @@ __device__ __forceinline__ void slot_meta(const DecodeParams& p, float tensor_sc
     return;
   }
   if (mode == 0) return;
-  bool good = true;
-  if (p.scale_mode == EKV_SCALE_PER_TENSOR) {
-    good = scale_ok(tensor_scale);
-#pragma unroll
-    for (int h = 0; h < kMaxKvHeads; ++h) m.sc[h] = tensor_scale;
-  } else {
-#pragma unroll
-    for (int h = 0; h < kMaxKvHeads; ++h) {
-      if (h < p.Hkv) {
-        m.sc[h] = __ldg(p.v_scales + (size_t)page * p.Hkv + h);
-        good = good && scale_ok(m.sc[h]);
-      }
-    }
-  }
-  if (good) {
+  const float s = p.scale_mode == EKV_SCALE_PER_TENSOR ? tensor_scale
+                                                         : __ldg(p.v_scales + (size_t)page * p.Hkv + h);
+  if (scale_ok(s)) {
     m.flags = kMetaCompact;
+    m.scale = s;
   } else {
     report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_SCALE, b);
     mark_bad(p, b);
@@ -161,106 +150,84 @@ __device__ __forceinline__ void slot_meta(const DecodeParams& p, float tensor_sc
   }
 }
 
-// The producer walks its range 32 slots at a time, one slot per lane. Metadata is
-// software-pipelined: while batch k is issued, the block-table entries of batch k+2
-// and the mode bytes / scales of batch k+1 are already in flight, so no TMA issue
-// waits on a dependent global load.
+// ------------------------------------------------------------------- warp rings
+struct WarpRing {
+  uint8_t* slots;       // this warp's nsl slots
+  uint64_t* full;       // this warp's nsl barriers (one arrive + bytes per fill)
+  int nsl;
+};
+
+__device__ __forceinline__ WarpRing warp_ring(const DecodeParams& p, uint8_t* smem, int slot_bytes) {
+  const int warp = threadIdx.x >> 5;
+  WarpRing r;
+  r.slots = smem + (size_t)warp * p.nsl * slot_bytes;
+  r.full = reinterpret_cast<uint64_t*>(smem + p.bar_off) + warp * p.nsl;
+  r.nsl = p.nsl;
+  return r;
+}
+
+// Fill the ring slot of page k (metadata page/flags broadcast by the caller): lane 0
+// arms the slot's barrier with the slice's bytes, then lanes issue the boxes.
 template <int D, int VMODE>
-__device__ void produce(const DecodeParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV8,
-                        const CUtensorMap* tmV16, uint8_t* stages, PageMeta* meta,
-                        uint64_t* full, uint64_t* empty, const int* cu, int start, int end) {
-  using L = StageLayout<D, VMODE>;
+__device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, int page, int flags,
+                                           const CUtensorMap* tmK, const CUtensorMap* tmV8,
+                                           const CUtensorMap* tmV16) {
+  using S = Slot<D, VMODE>;
+  constexpr int KB = D / 64;
   const int lane = threadIdx.x & 31;
-  const int NG = p.NG, Hkv = p.Hkv;
-  const int n_range = end - start;
-  const int n_slots = (n_range + NG - 1) / NG * NG;
-  const int k_sub = L::kKStage / NG;
-  const int v_sub = L::kVStage / NG;
-  const uint32_t k_bytes = kPage * Hkv * D * 2;
-  const uint32_t v8_bytes = kPage * Hkv * D;
-  const uint32_t v16_bytes = kPage * Hkv * D * 2;
+  const int s = k % ring.nsl;
+  uint64_t* bar = &ring.full[s];
+  const bool compact = (flags & kMetaCompact) != 0;
   if (lane == 0) {
-    tma_prefetch_desc(tmK);
-    if (VMODE != kVFP16) tma_prefetch_desc(tmV8);
-    if (VMODE != kVE4M3) tma_prefetch_desc(tmV16);
+    if (flags & kMetaSkip) mbar_arrive(bar);
+    else mbar_arrive_expect_tx(bar, S::kK + (compact ? kPage * D : kPage * D * 2));
   }
-  const float tensor_scale =
-      (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR) ? __ldg(p.v_scales) : 1.f;
-  SlotMeta cur, nxt, nxt2;
-  slot_ids(p, cu, start, n_range, lane, cur);
-  slot_ids(p, cu, start, n_range, 32 + lane, nxt);
-  slot_meta<VMODE>(p, tensor_scale, cur);
-  bool ok = true;
-  int last_si = -1;
-  for (int base = 0; base < n_slots && ok; base += 32) {
-    slot_ids(p, cu, start, n_range, base + 64 + lane, nxt2);
-    slot_meta<VMODE>(p, tensor_scale, nxt);
-    const int n_here = min(32, n_slots - base);
-    for (int i = 0; i < n_here; ++i) {
-      const int ri = base + i;
-      const int si = ri / NG, sub = ri - si * NG;
-      const int stage = si % L::kStages;
-      const uint32_t ph = (uint32_t)(si / L::kStages) & 1u;
-      if (sub == 0) {
-        int w = 1;
-        if (lane == 0) w = mbar_wait(&empty[stage], ph ^ 1u) ? 1 : 0;
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) {
-          if (lane == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_TIMEOUT, blockIdx.x);
-          ok = false;
-          break;
-        }
-      }
-      // lane i publishes the slot's metadata and the expected bytes; then the warp's
-      // lanes issue the page's TMA boxes in parallel, one box per lane
-      const int pg = __shfl_sync(0xffffffffu, cur.page, i);
-      const int fl = __shfl_sync(0xffffffffu, cur.flags, i);
-      if (lane == i) {
-        PageMeta& mt = meta[stage * 8 + sub];
-        mt.page = cur.page;
-        mt.ntok = cur.ntok;
-        mt.flags = cur.flags;
-#pragma unroll
-        for (int h = 0; h < kMaxKvHeads; ++h) mt.scale[h] = cur.sc[h];
-        if (cur.flags & kMetaSkip) {
-          mbar_arrive(&full[stage]);
-        } else {
-          const bool compact = (cur.flags & kMetaCompact) != 0;
-          mbar_arrive_expect_tx(&full[stage], k_bytes + (compact ? v8_bytes : v16_bytes));
-        }
-      }
-      __syncwarp();
-      if (!(fl & kMetaSkip)) {
-        const bool compact = (fl & kMetaCompact) != 0;
-        uint8_t* kd = stages + stage * L::kStageBytes + sub * k_sub;
-        uint8_t* vd = stages + stage * L::kStageBytes + L::kKStage + sub * v_sub;
-        const int nk = (D / 64) * Hkv;                      // K boxes: (column block, head)
-        const int nv = compact ? Hkv : (D / 64) * Hkv;      // V boxes
-        if (lane < nk) {
-          const int kb = lane / Hkv, hh = lane - kb * Hkv;
-          tma_load_4d(kd + lane * 2048, tmK, kb * 64, hh, 0, pg, &full[stage]);
-        } else if (lane < nk + nv) {
-          const int k = lane - nk;
-          if (compact) {
-            tma_load_4d(vd + k * (kPage * D), tmV8, 0, k, 0, pg, &full[stage]);
-          } else {
-            const int kb = k / Hkv, hh = k - kb * Hkv;
-            tma_load_4d(vd + k * 2048, tmV16, kb * 64, hh, 0, pg, &full[stage]);
-          }
-        }
-      }
-      __syncwarp();
-      last_si = si;
+  __syncwarp();
+  if (flags & kMetaSkip) return;
+  uint8_t* dst = ring.slots + (size_t)s * S::kBytes;
+  if (lane < KB) {
+    tma_load_4d(dst + lane * 2048, tmK, lane * 64, h, 0, page, bar);
+  } else if (lane < 2 * KB) {
+    const int kb = lane - KB;
+    if (compact) {
+      if (kb == 0) tma_load_4d(dst + S::kK, tmV8, 0, h, 0, page, bar);
+    } else {
+      tma_load_4d(dst + S::kK + kb * 2048, tmV16, kb * 64, h, 0, page, bar);
     }
-    cur = nxt;
-    nxt = nxt2;
   }
-  // No copy may still be landing in shared memory when the CTA exits: wait (bounded)
-  // for the last fills. In normal operation the consumers already saw them complete.
-  if (lane == 0 && last_si >= 0) {
-    for (int si = max(0, last_si - L::kStages + 1); si <= last_si; ++si)
-      mbar_wait(&full[si % L::kStages], (uint32_t)(si / L::kStages) & 1u);
+}
+
+// Order this warp's generic-proxy reads of a slot before the TMA (async-proxy) writes
+// that refill it.
+__device__ __forceinline__ void fence_reads_before_refill() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Common prologue of the split kernels: plan, this CTA's page range, barriers.
+// Returns false when the CTA has no pages.
+__device__ __forceinline__ bool split_prologue(const DecodeParams& p, uint8_t* smem, int* warp_tot, int& start,
+                                               int& end, int& per, int& b_first, int& b_last) {
+  int* cu = reinterpret_cast<int*>(smem + p.cu_off);
+  const int total = plan_pages(p, cu, warp_tot);
+  per = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+  if (blockIdx.x == 0) write_empty_sequences(p, cu);
+  start = (int)blockIdx.x * per;
+  end = min(total, start + per);
+  if (start >= end) return false;
+  if (threadIdx.x < kWarps * p.nsl) {
+    mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + threadIdx.x, 1);
+    fence_barrier_init();
   }
+  __syncthreads();
+  b_first = upper_bound_i(cu, p.batch + 1, start) - 1;
+  b_last = upper_bound_i(cu, p.batch + 1, end - 1) - 1;
+  return true;
+}
+
+// Aligned dynamic shared memory of the split kernels.
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* smem_raw) {
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  return smem_raw + pad;
 }
 
 // ------------------------------------------------------------------ fused merge
