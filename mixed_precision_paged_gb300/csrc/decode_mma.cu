@@ -64,6 +64,13 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   return v;
 }
 
+// 2^x with the MUFU approximation (flush-to-zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 __device__ __forceinline__ uint32_t e4m3_pair_to_h2(uint32_t two_codes) {
@@ -192,7 +199,34 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
           }
         }
       }
-      // the slice is in registers: refill the slot with this warp's page k + nsl
+      // ---- QK on the tensor cores (four independent accumulation chains), and the V
+      // rows turned into PV A fragments: after this the slot's data lives in registers
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t va[MT][4];
+      if (!skip) {
+        float sx[3][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+          float (&acc4)[4] = (s & 3) == 0 ? sc : sx[(s & 3) - 1];
+          mma_f16(acc4, kf[s][0], kf[s][1], kf[s][2], kf[s][3], qb[s][0], qb[s][1]);
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) sc[x] += (sx[0][x] + sx[1][x]) + sx[2][x];
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+          if (compact) {
+            const uint32_t* rr = vr[i >> 1];
+            e4m3_rows(rr[(i & 1) * 2], va[i][0], va[i][1]);
+            e4m3_rows(rr[(i & 1) * 2 + 1], va[i][2], va[i][3]);
+          } else {
+            va[i][0] = __byte_perm(vr[i][0], vr[i][1], 0x5410);
+            va[i][1] = __byte_perm(vr[i][0], vr[i][1], 0x7632);
+            va[i][2] = __byte_perm(vr[i][2], vr[i][3], 0x5410);
+            va[i][3] = __byte_perm(vr[i][2], vr[i][3], 0x7632);
+          }
+        }
+      }
+      // the slice is consumed from shared memory: refill the slot with page k + nsl
       fence_reads_before_refill();
       __syncwarp();
       {
@@ -205,16 +239,6 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
         }
       }
       if (!skip) {
-        // ---- QK on the tensor cores: two independent accumulation chains
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-        float sd[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s = 0; s < KS; ++s) {
-          if (s & 1) mma_f16(sd, kf[s][0], kf[s][1], kf[s][2], kf[s][3], qb[s][0], qb[s][1]);
-          else mma_f16(sc, kf[s][0], kf[s][1], kf[s][2], kf[s][3], qb[s][0], qb[s][1]);
-        }
-#pragma unroll
-        for (int x = 0; x < 4; ++x) sc[x] += sd[x];
         // rows r8 and r8 + 8 (tokens), cols 2q4, 2q4 + 1 (query heads)
         const bool v_lo = r8 < ntok, v_hi = r8 + 8 < ntok;
         const float s00 = v_lo ? sc[0] * p.qscale : -INFINITY;
@@ -228,10 +252,10 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
         }
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const __half2 plo = __floats2half2_rn(exp2f(s00 - mn0), exp2f(s01 - mn1));   // token r8
-        const __half2 phi = __floats2half2_rn(exp2f(s10 - mn0), exp2f(s11 - mn1));   // token r8+8
+        const __half2 plo = __floats2half2_rn(ex2(s00 - mn0), ex2(s01 - mn1));   // token r8
+        const __half2 phi = __floats2half2_rn(ex2(s10 - mn0), ex2(s11 - mn1));   // token r8+8
         if (__any_sync(0xffffffffu, (mn0 > m0) || (mn1 > m1))) {
-          const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+          const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
           l0 *= al0;
           l1 *= al1;
 #pragma unroll
@@ -261,17 +285,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
         const bool scaled = compact && !uniform_scale;
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
-          uint32_t a0, a1, a2, a3;
-          if (compact) {
-            const uint32_t* rr = vr[i >> 1];
-            e4m3_rows(rr[(i & 1) * 2], a0, a1);
-            e4m3_rows(rr[(i & 1) * 2 + 1], a2, a3);
-          } else {
-            a0 = __byte_perm(vr[i][0], vr[i][1], 0x5410);
-            a1 = __byte_perm(vr[i][0], vr[i][1], 0x7632);
-            a2 = __byte_perm(vr[i][2], vr[i][3], 0x5410);
-            a3 = __byte_perm(vr[i][2], vr[i][3], 0x7632);
-          }
+          uint32_t a0 = va[i][0], a1 = va[i][1], a2 = va[i][2], a3 = va[i][3];
           a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi;
           if (scaled) {
             // per-page scale in fp32 on this page's product
