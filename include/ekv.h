@@ -164,6 +164,35 @@ ekv_status ekv_demote_pages(ekv_ctx* ctx, void* v_pages, long long v_page_stride
                             int num_pages, const int32_t* page_ids, int n,
                             uint8_t* page_mode, float* scale_out, void* stream);
 
+/* Paged decode that allocates nothing, for callers that must not call cudaMalloc on
+ * this path (a runtime whose pool owns all device memory, an enqueue hook of a host
+ * framework that forbids allocation, a fixed start-up memory budget). The pages have
+ * no counterpart of this call: it computes exactly what ekv_paged_decode computes, for
+ * the shape given in its first three arguments, without a context.
+ *
+ * Its split-K scratch (partial records, tickets, flags) is one 16 MiB array of device
+ * memory compiled into the library: every GPU that loads the library holds it until
+ * the process exits. A call whose records need more than fits returns
+ * EKV_ERR_CAPACITY ((batch + #SMs) * (8 / H_kv) * H_q * (D + 2) floats plus 256 KiB of
+ * flags must fit in 16 MiB; batch <= 4096).
+ *  - The first call on a device looks up the array's device address (and the SM
+ *    count) with that device current; make that first call before any stream capture.
+ *  - Every call shares the one array and starts by clearing its flags on `stream`:
+ *    calls that overlap on the GPU (other streams, other host threads) race on it.
+ *  - err_out: device int[4] that receives {ekv_status, ekv_detail, index, 0} of the
+ *    first data error the kernel finds (zeroed by the call first), or NULL.
+ * No cudaMalloc, cudaFree or allocating library call is made; work is enqueued on
+ * `stream` (cudaMemsetAsync of the flags and err_out, then one kernel launch). The
+ * other arguments and all layouts are those of ekv_paged_decode. */
+ekv_status ekv_paged_decode_noalloc(int num_q_heads, int num_kv_heads, int head_dim,
+                                    const void* q, const void* k_pages, const void* v_pages,
+                                    long long v_page_stride_bytes, int num_pages,
+                                    const float* v_scales, int scale_mode,
+                                    const uint8_t* page_mode, int uniform_mode,
+                                    const int32_t* block_table, int block_table_stride,
+                                    const int32_t* seq_lens, int batch, float sm_scale,
+                                    void* out, float* lse, int* err_out, void* stream);
+
 /* Synchronise the stream of the context's last call, read the sticky device error
  * word and clear it. *code is an ekv_status (EKV_OK or EKV_ERR_DEVICE_CHECK), *detail
  * an ekv_detail. Either pointer may be NULL. Returns EKV_ERR_CUDA if the sync fails. */

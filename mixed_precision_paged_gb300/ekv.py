@@ -44,7 +44,8 @@ EKV_DETAIL_PAGE_MODE = 6
 
 EXPORTED = ["ekv_create", "ekv_destroy", "ekv_paged_decode", "ekv_gather_prefill",
             "ekv_demote_pages", "ekv_get_error", "ekv_profile_enable", "ekv_profile_read",
-            "ekv_set_decode_variant", "ekv_query", "ekv_status_string"]
+            "ekv_set_decode_variant", "ekv_query", "ekv_paged_decode_noalloc",
+            "ekv_status_string"]
 
 
 class ekv_config(ctypes.Structure):
@@ -63,6 +64,8 @@ _lib.ekv_paged_decode.argtypes = [_vp, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i,
 _lib.ekv_gather_prefill.argtypes = [_vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i, _i, _vp,
                                     _i, _vp, _vp, _vp, _i, _i, _vp]
 _lib.ekv_demote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
+_lib.ekv_paged_decode_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i,
+                                          _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp]
 _lib.ekv_get_error.argtypes = [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]
 _lib.ekv_profile_enable.argtypes = [_vp, _i]
 _lib.ekv_profile_read.argtypes = [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_ll)]
@@ -127,6 +130,21 @@ def ekv_paged_decode(ctx, q, k_pages, v_pages, v_page_stride_bytes, num_pages, v
                                  uniform_mode, _ptr(block_table), block_table_stride,
                                  _ptr(seq_lens), batch, float(sm_scale), _ptr(out), _ptr(lse),
                                  _stream(stream)), "ekv_paged_decode")
+
+
+def ekv_paged_decode_noalloc(num_q_heads, num_kv_heads, head_dim, q, k_pages, v_pages,
+                             v_page_stride_bytes, num_pages, v_scales, scale_mode, page_mode,
+                             uniform_mode, block_table, block_table_stride, seq_lens, batch,
+                             sm_scale, out, lse=None, err_out=None, stream=None):
+    """Decode with no context and no device allocation: the split-K scratch is a fixed
+    array inside the library (see include/ekv.h). For callers that may not allocate
+    device memory on this path."""
+    _check(_lib.ekv_paged_decode_noalloc(num_q_heads, num_kv_heads, head_dim, _ptr(q), _ptr(k_pages),
+                                         _ptr(v_pages), v_page_stride_bytes, num_pages, _ptr(v_scales),
+                                         scale_mode, _ptr(page_mode), uniform_mode, _ptr(block_table),
+                                         block_table_stride, _ptr(seq_lens), batch, float(sm_scale),
+                                         _ptr(out), _ptr(lse), _ptr(err_out), _stream(stream)),
+           "ekv_paged_decode_noalloc")
 
 
 def ekv_gather_prefill(ctx, k_pages, v_pages, v_page_stride_bytes, num_pages, v_scales,
