@@ -120,4 +120,19 @@ __device__ __forceinline__ uint16_t float2_to_e4m3x2(float x, float y) {
 
 __device__ __forceinline__ bool scale_ok(float s) { return s > 0.f && s <= 3.0e38f; }
 
+// x / s rounded to nearest-even in fp32, from r = the correctly rounded reciprocal of s:
+// q0 = RN(x * r) is within one ulp of x / s, the remainder x - q0 * s is exact in one
+// FMA, and RN(q0 + rem * r) is the correctly rounded quotient (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J.
+// Res. Dev. 34(1), 1990; Muller et al., Handbook of Floating-Point Arithmetic, Sec. 4.7).
+// The sign of a zero quotient is restored from x (s > 0). Valid while nothing
+// overflows or underflows: s a positive normal float, |x / s| far from the fp32 limits,
+// which holds for fp16 x and s = absmax / 448 of fp16 values. The unit test checks it
+// bit for bit against __fdiv_rn over that whole domain.
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float rem = __fmaf_rn(-q0, s, x);
+  return copysignf(__fmaf_rn(rem, r, q0), x);
+}
+
 }  // namespace ekv

@@ -115,13 +115,16 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
 // ElasticKV Sec. 3.4: synchronous in-place demotion; the page reads as compact only
 // after the kernel completes (stream order publishes codes, scales and mode together).
 // Per KV head h: a = max|x|, s = a / 448 (IEEE fp32 divide; 1 when a == 0),
-// code = E4M3_rn_satfinite(x / s). The whole FP16 page is loaded into registers
-// before the first barrier, so the codes may overwrite the page's first half.
+// code = E4M3_rn_satfinite(x / s). The quotient is the IEEE one, computed by
+// div_by_scale (reciprocal + one Markstein correction; checked against __fdiv_rn).
+// The whole FP16 page is loaded into registers before the first barrier, so the
+// codes may overwrite the page's first half.
 __global__ void __launch_bounds__(256, 4)
 demote_kernel(const DemoteParams p) {
   constexpr int kMaxVec = 8;                      // 8 x 16 B x 256 = 32 KiB (H_kv*D <= 1024)
   __shared__ unsigned int s_amax[kMaxKvHeads];
   __shared__ float s_scale[kMaxKvHeads];
+  __shared__ float s_recip[kMaxKvHeads];
   __shared__ int s_nonfinite;
   const int tid = threadIdx.x, lane = tid & 31;
   const int page = __ldg(p.page_ids + blockIdx.x);
@@ -172,7 +175,9 @@ demote_kernel(const DemoteParams p) {
       s_nonfinite = 1;
     } else {
       const float a = __half2float(__ushort_as_half((unsigned short)bits));
-      s_scale[tid] = a == 0.f ? 1.f : __fdiv_rn(a, 448.f);
+      const float sc = a == 0.f ? 1.f : __fdiv_rn(a, 448.f);
+      s_scale[tid] = sc;
+      s_recip[tid] = __frcp_rn(sc);
     }
   }
   __syncthreads();
@@ -185,15 +190,15 @@ demote_kernel(const DemoteParams p) {
     const int v = tid + u * 256;
     if (v >= nvec) break;
     const int head = ((v * 8) / p.D) % p.Hkv;
-    const float s = s_scale[head];
+    const float s = s_scale[head], rs = s_recip[head];
     const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
     uint32_t packed[2];
 #pragma unroll
     for (int q = 0; q < 4; q += 2) {
       const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
       const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w[q + 1]));
-      const uint16_t lo = float2_to_e4m3x2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s));
-      const uint16_t hi = float2_to_e4m3x2(__fdiv_rn(b.x, s), __fdiv_rn(b.y, s));
+      const uint16_t lo = float2_to_e4m3x2(div_by_scale(a.x, s, rs), div_by_scale(a.y, s, rs));
+      const uint16_t hi = float2_to_e4m3x2(div_by_scale(b.x, s, rs), div_by_scale(b.y, s, rs));
       packed[q / 2] = (uint32_t)lo | ((uint32_t)hi << 16);
     }
     *reinterpret_cast<uint2*>(base + (size_t)v * 8) = make_uint2(packed[0], packed[1]);
