@@ -57,9 +57,10 @@ struct DecodeParams {
 constexpr int kMetaCompact = 1;
 constexpr int kMetaSkip = 2;
 
-// One ring slot holds one (page, KV head) slice: K [16][D] fp16 as D/64 TMA boxes of
-// 16 rows x 128 B, then V [16][D] as E4M3 rows (one box of 16 x D bytes) or fp16 (D/64
-// boxes). Slots are 1024-byte aligned, as the 128B swizzle requires.
+// One ring slot holds one (page, KV head) slice: K [16][D] fp16 as D/64 blocks of 16
+// rows x 128 B (one 5-D TMA box), then V [16][D] as E4M3 rows (one box of 16 x D
+// bytes) or fp16 (D/64 blocks, one box). Slots are 1024-byte aligned, as the 128B
+// swizzle requires.
 template <int D, int VMODE>
 struct Slot {
   static constexpr int kK = kPage * D * 2;

@@ -10,6 +10,7 @@
 
 #include "decode.cuh"
 #include "gather_demote.cuh"
+#include "pool_maps.h"
 
 namespace ekv {
 cudaError_t launch_split_simt(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
@@ -40,40 +41,6 @@ struct ekv_ctx {
 };
 
 namespace {
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// 4-D view (d, head, token-in-page, page) of a page pool; one box = 16 rows of one
-// KV head and `box_d` columns, landing [16][box_d * esz] in shared memory.
-bool encode_pool_map(CUtensorMap* tm, CUtensorMapDataType dt, int esz, const void* base, int D,
-                     int Hkv, int num_pages, long long page_stride, int box_d,
-                     CUtensorMapSwizzle sw) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)kPage, (cuuint64_t)num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)D * esz, (cuuint64_t)Hkv * D * esz, (cuuint64_t)page_stride};
-  cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)kPage, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(tm, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -139,7 +106,7 @@ ekv_status ekv_create(ekv_ctx** out, const ekv_config* cfg) {
             cudaMemset(c->plan, 0, kPlanInts * sizeof(int)) == cudaSuccess &&
             cudaMemset(c->err, 0, 4 * sizeof(int)) == cudaSuccess &&
             cudaDeviceSynchronize() == cudaSuccess;
-  if (!ok || !get_encode()) {
+  if (!ok || !encode_fn()) {
     ekv_destroy(c);
     return EKV_ERR_CUDA;
   }
@@ -192,19 +159,7 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
 
   DeviceGuard g(c->device);
   CUtensorMap tk, t8, t16;
-  memset(&tk, 0, sizeof(tk));
-  memset(&t8, 0, sizeof(t8));
-  memset(&t16, 0, sizeof(t16));
-  if (!encode_pool_map(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, k_pages, D, Hkv, num_pages,
-                       (long long)kPage * Hkv * D * 2, 64, CU_TENSOR_MAP_SWIZZLE_128B))
-    return EKV_ERR_INVALID_ARG;
-  if (vmode != kVFP16 &&
-      !encode_pool_map(&t8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, v_pages, D, Hkv, num_pages, v_page_stride_bytes, D,
-                       D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
-    return EKV_ERR_INVALID_ARG;
-  if (vmode != kVE4M3 &&
-      !encode_pool_map(&t16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, v_pages, D, Hkv, num_pages, v_page_stride_bytes,
-                       64, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!decode_pool_maps(&tk, &t8, &t16, k_pages, v_pages, D, Hkv, num_pages, v_page_stride_bytes, vmode))
     return EKV_ERR_INVALID_ARG;
 
   DecodeParams p;

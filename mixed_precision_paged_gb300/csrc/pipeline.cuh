@@ -14,9 +14,11 @@
 // Rings: warp w owns KV head h = w % Hkv and page group grp = w / Hkv (NG = 8 / Hkv
 // groups): it handles the slices (page r, head h) of the CTA's pages r = grp, grp + NG,
 // ... in order. Each warp keeps its own ring of `nsl` slots in shared memory and feeds
-// it itself: one TMA box per 64-column block of K and of V, 128B/64B-swizzled so that
-// the warp's 16-byte row reads are bank-conflict free. No warp waits for another, and a
-// slot is refilled as soon as its owner has pulled the slice into registers.
+// it itself: lane 0 issues one TMA box for the K slice and one for the V slice,
+// 128B/64B-swizzled so that the warp's 16-byte row reads are bank-conflict free. A bulk
+// tensor copy stalls its issuing warp for about the same time whatever its size, so
+// each slice is a single box. No warp waits for another, and a slot is refilled as soon
+// as its owner has pulled the slice into registers.
 #pragma once
 
 #include "decode.cuh"
@@ -166,35 +168,28 @@ __device__ __forceinline__ WarpRing warp_ring(const DecodeParams& p, uint8_t* sm
   return r;
 }
 
-// Fill the ring slot of page k (metadata page/flags broadcast by the caller): lane 0
-// arms the slot's barrier with the slice's bytes, then lanes issue the boxes.
+// Fill the ring slot of page k (metadata page/flags broadcast by the caller). Lane 0
+// arms the slot's barrier with the slice's bytes and issues one bulk tensor copy per
+// tensor: K through the 5-D fp16 slice map, V through the E4M3 map (compact page) or
+// the fp16 slice map (TARGET page). A skipped page only arrives on the barrier.
 template <int D, int VMODE>
 __device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, int page, int flags,
                                            const CUtensorMap* tmK, const CUtensorMap* tmV8,
                                            const CUtensorMap* tmV16) {
   using S = Slot<D, VMODE>;
-  constexpr int KB = D / 64;
-  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x & 31) != 0) return;
   const int s = k % ring.nsl;
   uint64_t* bar = &ring.full[s];
-  const bool compact = (flags & kMetaCompact) != 0;
-  if (lane == 0) {
-    if (flags & kMetaSkip) mbar_arrive(bar);
-    else mbar_arrive_expect_tx(bar, S::kK + (compact ? kPage * D : kPage * D * 2));
+  if (flags & kMetaSkip) {
+    mbar_arrive(bar);
+    return;
   }
-  __syncwarp();
-  if (flags & kMetaSkip) return;
+  const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (flags & kMetaCompact));
   uint8_t* dst = ring.slots + (size_t)s * S::kBytes;
-  if (lane < KB) {
-    tma_load_4d(dst + lane * 2048, tmK, lane * 64, h, 0, page, bar);
-  } else if (lane < 2 * KB) {
-    const int kb = lane - KB;
-    if (compact) {
-      if (kb == 0) tma_load_4d(dst + S::kK, tmV8, 0, h, 0, page, bar);
-    } else {
-      tma_load_4d(dst + S::kK + kb * 2048, tmV16, kb * 64, h, 0, page, bar);
-    }
-  }
+  mbar_arrive_expect_tx(bar, S::kK + (compact ? kPage * D : kPage * D * 2));
+  tma_load_5d(dst, tmK, 0, 0, 0, h, page, bar);
+  if (compact) tma_load_4d(dst + S::kK, tmV8, 0, h, 0, page, bar);
+  else tma_load_5d(dst + S::kK, tmV16, 0, 0, 0, h, page, bar);
 }
 
 // Order this warp's generic-proxy reads of a slot before the TMA (async-proxy) writes
