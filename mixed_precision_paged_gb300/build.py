@@ -31,7 +31,7 @@ def nvcc():
 
 
 def _inputs():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh"))]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))]
     return files + [os.path.join(INCLUDE, "ekv.h"), os.path.abspath(__file__)]
 
 
