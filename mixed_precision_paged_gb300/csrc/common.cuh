@@ -107,6 +107,17 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* tm, in
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (cp.async, LSU path), and the
+// wait for all of this thread's such copies.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Byte offset inside a 1024-byte-aligned TMA box after the hardware swizzle:
 // 128B mode XORs the 16-byte chunk index (bits 4..6) with bits 7..9, 64B mode XORs
 // bits 4..5 with bits 7..8.

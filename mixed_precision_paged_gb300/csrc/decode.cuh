@@ -20,13 +20,11 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSlots = 32;                          // ring slots per warp
 constexpr int kSplitSmemMax = 232448 - 1024;           // dynamic smem opt-in (static smem < 1 KB)
 
-// plan buffer (int32), zeroed at context creation:
-//   [kPlanBad + b * 8 + h]    set when sequence b read bad data (page id, mode, scale);
-//                             the merge of (b, h) zeroes the output and clears it
-//   [kPlanTicket + b * 8 + h] partial records written so far for (b, KV head h); the
-//                             warp that brings it to its final count merges and resets it
-constexpr int kPlanBad = 0;
-constexpr int kPlanTicket = kPlanBad + kMaxBatch * kMaxKvHeads;
+// plan buffer (int32), zeroed at context creation and left zeroed by every launch:
+//   [kPlanTicket + b * 8 + h] partial records counted so far for (b, KV head h) of a
+//                             sequence split across CTAs; the warp that brings it to
+//                             its final count merges and resets it
+constexpr int kPlanTicket = 0;
 constexpr int kPlanInts = kPlanTicket + kMaxBatch * kMaxKvHeads;
 
 struct DecodeParams {

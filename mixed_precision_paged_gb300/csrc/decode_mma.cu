@@ -122,6 +122,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
   wm_meta<VMODE>(p, tensor_scale, h, nxt);
   wm_ids(p, cu, start, n_my, grp, 64 + lane, nxt2);
   int k = 0;                                        // next page of this warp
+  bool timed_out = false;
 
   for (int b = b_first; b <= b_last; ++b) {
     const int j0 = max(cu[b], start), j1 = min(cu[b + 1], end);
@@ -142,6 +143,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
     for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY;           // running max of g = 2q4, 2q4 + 1
     float l0 = 0.f, l1 = 0.f;                       // this lane's share of the sums
+    bool seg_bad = false;                           // a page of this segment was skipped
     const int r_end = j1 - start;
     for (; k < n_my && grp + k * NG < r_end; ++k) {
       if ((k & 31) == 0 && k > 0) {                 // next metadata batch
@@ -156,13 +158,15 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
         // drain this warp's other fills in flight (bounded), then stop
         for (int kk = k + 1; kk < min(k + ring.nsl, n_my); ++kk)
           mbar_wait(&ring.full[kk % ring.nsl], (uint32_t)(kk / ring.nsl) & 1u);
-        return;
+        timed_out = true;
+        break;
       }
       const int flags = __shfl_sync(0xffffffffu, cur.flags, k & 31);
       const int ntok = __shfl_sync(0xffffffffu, cur.ntok, k & 31);
       const float pscale = __shfl_sync(0xffffffffu, cur.scale, k & 31);
       const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (flags & kMetaCompact));
       const bool skip = (flags & kMetaSkip) != 0;
+      seg_bad |= skip;
       const float vs = (compact && !uniform_scale) ? pscale : 1.f;
       // Pull this (page, head) slice into registers and refill its slot at once, so
       // that the next fill is in flight while the tiles are multiplied: K as QK A
@@ -301,7 +305,9 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
         }
       }
     }
-    // ---- partial record (natural d order)
+    if (timed_out) break;
+    // ---- segment end (natural d order): the finished output when this warp saw the
+    // whole sequence (NG = 1 and no other CTA touches it), else a partial record
     float lt0 = l0, lt1 = l1;
 #pragma unroll
     for (int o = 4; o <= 16; o <<= 1) {
@@ -309,8 +315,27 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
       lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
     }
     const float us = uniform_scale ? __ldg(p.v_scales) : 1.f;
-    const size_t R = (size_t)(b + blockIdx.x) * NG + grp;
     const int g0 = 2 * q4, g1 = 2 * q4 + 1;
+    if (seg_bad) lt0 = lt1 = kBadRecord;
+    if (NG == 1 && !crosses_ctas(cu, b, start, end)) {
+      const float i0 = lt0 > 0.f ? us / lt0 : 0.f, i1 = lt1 > 0.f ? us / lt1 : 0.f;
+      __half* ob = p.out + ((size_t)b * p.Hq + h * G) * D;
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        const int d = 16 * i + 2 * r8;
+        if (g0 < G)
+          *reinterpret_cast<__half2*>(ob + g0 * D + d) = __floats2half2_rn(acc[i][0] * i0, acc[i][2] * i0);
+        if (g1 < G)
+          *reinterpret_cast<__half2*>(ob + g1 * D + d) = __floats2half2_rn(acc[i][1] * i1, acc[i][3] * i1);
+      }
+      if (r8 == 0 && p.lse) {
+        float* lb = p.lse + (size_t)b * p.Hq + h * G;
+        if (g0 < G) lb[g0] = lt0 > 0.f ? (m0 + log2f(lt0)) * 0.69314718055994531f : -INFINITY;
+        if (g1 < G) lb[g1] = lt1 > 0.f ? (m1 + log2f(lt1)) * 0.69314718055994531f : -INFINITY;
+      }
+      continue;
+    }
+    const size_t R = (size_t)(b + blockIdx.x) * NG + grp;
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
       const int d = 16 * i + 2 * r8;
@@ -325,8 +350,8 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
       if (g0 < G) p.part_ml[R * p.Hq + h * G + g0] = make_float2(m0, lt0);
       if (g1 < G) p.part_ml[R * p.Hq + h * G + g1] = make_float2(m1, lt1);
     }
-    finish_segment<D>(p, b, h, cu, per);
   }
+  finish_warp<D>(p, cu, start, end, per, b_first, b_last, h, grp, merge_buf(ring, S::kBytes));
 }
 
 template <int D, int VMODE>

@@ -46,6 +46,7 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
   wm_meta<VMODE>(p, tensor_scale, h, nxt);
   wm_ids(p, cu, start, n_my, grp, 64 + lane, nxt2);
   int k = 0;
+  bool timed_out = false;
 
   for (int b = b_first; b <= b_last; ++b) {
     const int j0 = max(cu[b], start), j1 = min(cu[b + 1], end);
@@ -76,6 +77,7 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
 #pragma unroll
       for (int x = 0; x < VPL; ++x) acc[g][x] = 0.f;
     }
+    bool seg_bad = false;                          // a page of this segment was skipped
     const int r_end = j1 - start;
     for (; k < n_my && grp + k * NG < r_end; ++k) {
       if ((k & 31) == 0 && k > 0) {
@@ -89,11 +91,13 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
         if (lane == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_TIMEOUT, blockIdx.x);
         for (int kk = k + 1; kk < min(k + ring.nsl, n_my); ++kk)
           mbar_wait(&ring.full[kk % ring.nsl], (uint32_t)(kk / ring.nsl) & 1u);
-        return;
+        timed_out = true;
+        break;
       }
       const int mflags = __shfl_sync(0xffffffffu, cur.flags, k & 31);
       const int mntok = __shfl_sync(0xffffffffu, cur.ntok, k & 31);
       const float mscale = __shfl_sync(0xffffffffu, cur.scale, k & 31);
+      seg_bad |= (mflags & kMetaSkip) != 0;
       if (!(mflags & kMetaSkip)) {
         const uint8_t* kp = ring.slots + (size_t)s_idx * S::kBytes;
         const uint8_t* vp = kp + S::kK;
@@ -199,7 +203,10 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
         ring_issue<D, VMODE>(ring, kk, h, pg, fl, tmK, tmV8, tmV16);
       }
     }
-    // partial record of (segment b, this CTA, page group grp) for this KV head's G heads
+    if (timed_out) break;
+    // the finished output when this warp saw the whole sequence (NG = 1 and no other
+    // CTA touches it), else the partial record of (segment b, this CTA, page group grp)
+    const bool direct = NG == 1 && !crosses_ctas(cu, b, start, end);
     const size_t R = (size_t)(b + blockIdx.x) * NG + grp;
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
@@ -207,6 +214,17 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
       float ls = l[g];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      if (seg_bad) ls = kBadRecord;
+      if (direct) {
+        const float inv = ls > 0.f ? 1.f / ls : 0.f;
+        __half* o = p.out + ((size_t)b * p.Hq + h * G + g) * D + lane * VPL;
+#pragma unroll
+        for (int x = 0; x < VPL; x += 2)
+          *reinterpret_cast<__half2*>(o + x) = __floats2half2_rn(acc[g][x] * inv, acc[g][(x + 1) % VPL] * inv);
+        if (lane == 0 && p.lse)
+          p.lse[(size_t)b * p.Hq + h * G + g] = ls > 0.f ? (m[g] + log2f(ls)) * 0.69314718055994531f : -INFINITY;
+        continue;
+      }
       float* dst = p.part_acc + (R * p.Hq + h * G + g) * D + lane * VPL;
       if (VPL == 4) {
         *reinterpret_cast<float4*>(dst) = make_float4(acc[g][0], acc[g][1 % VPL], acc[g][2 % VPL], acc[g][3 % VPL]);
@@ -215,8 +233,8 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
       }
       if (lane == 0) p.part_ml[R * p.Hq + h * G + g] = make_float2(m[g], ls);
     }
-    finish_segment<D>(p, b, h, cu, per);
   }
+  finish_warp<D>(p, cu, start, end, per, b_first, b_last, h, grp, merge_buf(ring, S::kBytes));
 }
 
 // --------------------------------------------------------------------- the kernel
@@ -267,8 +285,8 @@ static cudaError_t dispatch_simt_g(const CUtensorMap& tk, const CUtensorMap& t8,
 }
 
 // Shared-memory layout of a split launch: 8 rings of as many slots as fit next to the
-// barriers, the page prefix sums of `batch` sequences and (CUDA-core consumer) the
-// probability buffer. Returns the dynamic smem bytes to request.
+// barriers (one per slot), the page prefix sums of `batch` sequences and (CUDA-core
+// consumer) the probability buffer. Returns the dynamic smem bytes to request.
 template <int D, int VMODE>
 static size_t layout_for(DecodeParams& p, int algo) {
   using S = Slot<D, VMODE>;

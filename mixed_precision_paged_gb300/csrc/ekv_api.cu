@@ -309,7 +309,7 @@ ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {
   if (cudaMemcpy(h, c->err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return EKV_ERR_CUDA;
   if (cudaMemset(c->err, 0, sizeof(h)) != cudaSuccess) return EKV_ERR_CUDA;
   // after a device error (a kernel may have wound down early) start the next call from
-  // a clean plan buffer: no stale tickets or flags
+  // a clean plan buffer: no stale tickets
   if (h[0] != 0 && cudaMemset(c->plan, 0, kPlanInts * sizeof(int)) != cudaSuccess) return EKV_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return EKV_ERR_CUDA;
   if (code) *code = h[0];

@@ -120,10 +120,9 @@ extern "C" ekv_status ekv_paged_decode_noalloc(int num_q_heads, int num_kv_heads
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* plan = reinterpret_cast<int*>(ds.scratch);
   int* err = err_out ? err_out : reinterpret_cast<int*>(ds.scratch + kPlanBytes);
-  // The array keeps whatever the previous call left: clear the tickets and bad flags
-  // of this batch and the error word before the launch (records need no clearing).
-  if (cudaMemsetAsync(plan + kPlanBad, 0, (size_t)batch * kMaxKvHeads * 4, st) != cudaSuccess ||
-      cudaMemsetAsync(plan + kPlanTicket, 0, (size_t)batch * kMaxKvHeads * 4, st) != cudaSuccess ||
+  // The array keeps whatever the previous call left: clear the tickets of this batch
+  // and the error word before the launch (records need no clearing).
+  if (cudaMemsetAsync(plan + kPlanTicket, 0, (size_t)batch * kMaxKvHeads * 4, st) != cudaSuccess ||
       cudaMemsetAsync(err, 0, 4 * sizeof(int), st) != cudaSuccess)
     return EKV_ERR_CUDA;
 

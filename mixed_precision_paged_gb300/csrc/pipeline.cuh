@@ -9,7 +9,8 @@
 // writes one partial record per (segment, page group) at record (b + c) * NG + group,
 // which is unique because the CTAs that touch sequence b are exactly
 // cu[b]/per .. (cu[b+1]-1)/per and those ranges of consecutive sequences only meet
-// at one CTA.
+// at one CTA. Records are written without any synchronisation as segments end; the
+// merges happen when a warp's stream ends (finish_warp).
 //
 // Rings: warp w owns KV head h = w % Hkv and page group grp = w / Hkv (NG = 8 / Hkv
 // groups): it handles the slices (page r, head h) of the CTA's pages r = grp, grp + NG,
@@ -34,10 +35,6 @@ __device__ __forceinline__ int upper_bound_i(const int* a, int n, int x) {
   return lo;
 }
 
-__device__ __forceinline__ void mark_bad(const DecodeParams& p, int b) {
-  for (int h = 0; h < p.Hkv; ++h) p.plan[kPlanBad + b * kMaxKvHeads + h] = 1;
-}
-
 // Sequences with no pages (length 0, or a length the block table cannot hold) are
 // touched by no CTA: CTA 0 writes their zero output and -inf lse, reading the page
 // prefix sums already in shared memory (no global loads on this path).
@@ -52,8 +49,8 @@ __device__ __forceinline__ void write_empty_sequences(const DecodeParams& p, con
 }
 
 // Block-wide prefix sum of pages per sequence into cu[0..B]; returns the total.
-// Sequences with a length outside [0, bt_stride*16] count as empty and are reported
-// (by CTA 0 only) and flagged so that the merge zeroes them.
+// Sequences with a length outside [0, bt_stride*16] count as empty (CTA 0 writes their
+// zero output) and are reported by CTA 0.
 __device__ __forceinline__ int plan_pages(const DecodeParams& p, int* cu, int* warp_tot) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kNW = kThreads / 32;
@@ -128,14 +125,12 @@ __device__ __forceinline__ void wm_meta(const DecodeParams& p, float tensor_scal
   const int b = m.b, page = m.page;
   if (page < 0 || page >= p.num_pages) {
     report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, b);
-    mark_bad(p, b);
     m.flags = kMetaSkip;
     return;
   }
   const int mode = VMODE == kVE4M3 ? 1 : (VMODE == kVFP16 ? 0 : (int)__ldg(p.page_mode + page));
   if (mode > 1) {
     report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_MODE, b);
-    mark_bad(p, b);
     m.flags = kMetaSkip;
     return;
   }
@@ -147,7 +142,6 @@ __device__ __forceinline__ void wm_meta(const DecodeParams& p, float tensor_scal
     m.scale = s;
   } else {
     report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_SCALE, b);
-    mark_bad(p, b);
     m.flags = kMetaSkip;
   }
 }
@@ -166,6 +160,19 @@ __device__ __forceinline__ WarpRing warp_ring(const DecodeParams& p, uint8_t* sm
   r.full = reinterpret_cast<uint64_t*>(smem + p.bar_off) + warp * p.nsl;
   r.nsl = p.nsl;
   return r;
+}
+
+// The merge scratch of a warp: its ring, free once its stream has ended.
+struct MergeBuf {
+  uint8_t* buf;
+  int bytes;
+};
+
+__device__ __forceinline__ MergeBuf merge_buf(const WarpRing& ring, int slot_bytes) {
+  MergeBuf mb;
+  mb.buf = ring.slots;
+  mb.bytes = ring.nsl * slot_bytes;
+  return mb;
 }
 
 // Fill the ring slot of page k (metadata page/flags broadcast by the caller). Lane 0
@@ -209,8 +216,8 @@ __device__ __forceinline__ bool split_prologue(const DecodeParams& p, uint8_t* s
   start = (int)blockIdx.x * per;
   end = min(total, start + per);
   if (start >= end) return false;
-  if (threadIdx.x < kWarps * p.nsl) {
-    mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + threadIdx.x, 1);
+  for (int i = threadIdx.x; i < kWarps * p.nsl; i += blockDim.x) {
+    mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -226,117 +233,219 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* smem_raw) {
 }
 
 // ------------------------------------------------------------------ fused merge
-// Combine the partial records of sequence b for the G query heads of KV head h:
+// Partial results. A warp's result for (segment b, page group grp, KV head h) is
+//   m = max score (log2 units), l = sum 2^(s - m), acc = sum 2^(s - m) v
+// per query head. It is written as record (b + c) * NG + grp of CTA c, except when
+// the warp saw the whole sequence (NG = 1 and no other CTA touches it): then it writes
+// the finished output directly. A warp that met a page it must skip (bad id, mode
+// byte or scale) writes l = -1 instead: the merge turns that into a zero output and
+// lse = -inf for the query heads of h.
+constexpr float kBadRecord = -1.f;
+
+// A merge job: the records rec0 .. rec0 + nrec - 1 of (sequence b, KV head h).
+struct MergeJob {
+  int b;
+  int rec0;
+  int nrec;
+};
+
+// Combine the records of each job, in one pass with a running maximum:
 //   M = max m_i,  L = sum l_i 2^(m_i - M),  out = sum acc_i 2^(m_i - M) / L,
 //   lse = (M + log2 L) ln 2.
-// The warp's lanes split over (head, column block): 32/GP lanes per head read
-// their columns of every record with independent loads, so a merge costs a few L2
-// round trips whatever the record count. Records are read through L2 (ld.global.cg):
-// other SMs wrote them in this launch.
-template <int D>
-__device__ void merge_heads(const DecodeParams& p, int b, int h, int c0, int n_cta, bool bad) {
-  constexpr int kMaxDpl = D / 4;                     // columns per lane when G == 8
+// The records of consecutive jobs are staged together in `buf` (the warp's ring, idle
+// once its stream has ended), up to kMaxSlots per wave: the acc blocks (G x D floats
+// each, contiguous) by 16-byte cp.async copies spread over the lanes, the (m, l) pairs
+// by plain loads, all issued before any is used. A wave costs one L2 round trip
+// (freshly written records take ~2 us to come back), however many jobs and records it
+// holds; a job longer than a wave continues in the next one. (A 1-D bulk copy per
+// record would cost its issuing lane more than the round trip.) Lanes split over
+// (query head, column block): 32/GP lanes per head, kDpl columns each. A record with
+// l = 0 (a page group without tokens) contributes nothing; l < 0 marks a skipped page
+// and zeroes the output of its job.
+template <int D, int GP>
+__device__ void merge_jobs(const DecodeParams& p, int h, const MergeJob* jobs, int nj, uint8_t* buf,
+                           int buf_bytes) {
+  constexpr int kLph = 32 / GP;                      // lanes per query head
+  constexpr int kDpl = D / kLph;                     // columns per lane
+  constexpr int kMaxSlots = 16;
+  constexpr int kTables = kMaxSlots * 4 + kMaxSlots * 8 * 8;   // slot records, (m, l) pairs
   const int lane = threadIdx.x & 31;
-  const int G = p.G, NG = p.NG;
-  const int GP = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
-  const int lph = 32 / GP;                           // lanes per query head
-  const int g = lane / lph, sub = lane - g * lph;
-  const int dpl = D / lph;                           // columns per lane (2..32)
-  const int d0 = sub * dpl;
+  const int G = p.G;
+  const int g = lane / kLph, sub = lane % kLph, d0 = sub * kDpl;
   const bool active = g < G;
-  const int hq = h * G + (active ? g : 0);
-  const int nrec = n_cta * NG;
-  const unsigned gmask = 0xffffffffu;
-  __half* o = p.out + ((size_t)b * p.Hq + hq) * D + d0;
-  if (bad) {
-    if (active) {
-#pragma unroll
-      for (int x = 0; x < kMaxDpl; x += 2)
-        if (x < dpl) *reinterpret_cast<__half2*>(o + x) = __floats2half2_rn(0.f, 0.f);
-      if (sub == 0 && p.lse) p.lse[(size_t)b * p.Hq + hq] = -INFINITY;
-    }
+  const int gl = active ? g : 0;
+  const int rb = G * D * 4;                          // bytes of one record's acc block
+  int* slot_rec = reinterpret_cast<int*>(buf);
+  float2* slot_ml = reinterpret_cast<float2*>(buf + kMaxSlots * 4);   // [slot][8 heads]
+  uint8_t* slot_acc = buf + kTables;
+  int cap = (buf_bytes - kTables) / rb;
+  cap = cap > kMaxSlots ? kMaxSlots : cap;
+  if (cap < 1) {                                     // a ring smaller than one record: cannot happen
+    if (lane == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_TIMEOUT, blockIdx.x);
     return;
   }
-  // pass 1: max of m over the records (lanes of a head split the records)
-  float M = -INFINITY;
-  for (int i = sub; i < nrec; i += lph) {
-    const size_t R = (size_t)(b + c0 + i / NG) * NG + (i % NG);
-    const float2 ml = __ldcg(p.part_ml + R * p.Hq + hq);
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
-  }
-  for (int off = 1; off < lph; off <<= 1) M = fmaxf(M, __shfl_xor_sync(gmask, M, off));
-  // pass 2: weights, L and the weighted column sums
-  float acc[kMaxDpl];
-#pragma unroll
-  for (int x = 0; x < kMaxDpl; ++x) acc[x] = 0.f;
-  float Ls = 0.f;
-  for (int i0 = 0; i0 < nrec; i0 += lph) {
-    float w = 0.f;
-    {
-      const int i = i0 + sub;
-      if (i < nrec) {
-        const size_t R = (size_t)(b + c0 + i / NG) * NG + (i % NG);
-        const float2 ml = __ldcg(p.part_ml + R * p.Hq + hq);
-        if (ml.y > 0.f) {
-          w = exp2f(ml.x - M);
-          Ls = fmaf(w, ml.y, Ls);
-        }
+  float acc[kDpl];
+  float M = -INFINITY, L = 0.f;
+  bool bad = false;
+  int j = 0, r = 0;                                  // next record to stage
+  int cj = 0, cr = 0;                                // next record to combine
+  while (j < nj) {
+    // plan the wave (the same on every lane); lane 0 writes the slot table
+    __syncwarp();                                    // the previous wave is consumed
+    int ns = 0;
+    while (j < nj && ns < cap) {
+      if (lane == 0) slot_rec[ns] = jobs[j].rec0 + r;
+      ++ns;
+      if (++r == jobs[j].nrec) {
+        ++j;
+        r = 0;
       }
     }
-    const int n_here = min(lph, nrec - i0);
-    for (int j = 0; j < n_here; ++j) {
-      const float wj = __shfl_sync(gmask, w, g * lph + j);
-      if (wj == 0.f) continue;                       // uniform within the head's lanes
-      const int i = i0 + j;
-      const size_t R = (size_t)(b + c0 + i / NG) * NG + (i % NG);
-      const float* src = p.part_acc + (R * p.Hq + hq) * D + d0;
+    __syncwarp();
+    for (int s = 0; s < ns; ++s) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(p.part_acc + ((size_t)slot_rec[s] * p.Hq + h * G) * D);
+      for (int off = lane * 16; off < rb; off += 32 * 16) cp_async_16(slot_acc + s * rb + off, src + off);
+    }
+    float2 v[kMaxSlots * 8 / 32];
 #pragma unroll
-      for (int x = 0; x < kMaxDpl; x += 2) {
-        if (x < dpl) {
-          const float2 a = __ldcg(reinterpret_cast<const float2*>(src + x));
-          acc[x] = fmaf(wj, a.x, acc[x]);
-          acc[x + 1] = fmaf(wj, a.y, acc[x + 1]);
+    for (int i = 0; i < kMaxSlots * 8 / 32; ++i) {
+      const int q = lane + 32 * i;
+      v[i] = q < ns * G ? __ldcg(p.part_ml + (size_t)slot_rec[q / G] * p.Hq + h * G + q % G)
+                        : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxSlots * 8 / 32; ++i) {
+      const int q = lane + 32 * i;
+      if (q < ns * G) slot_ml[(q / G) * 8 + q % G] = v[i];
+    }
+    cp_async_wait_all();
+    __syncwarp();                                    // every lane's copies and pairs visible
+    for (int s = 0; s < ns; ++s) {
+      if (cr == 0) {
+#pragma unroll
+        for (int x = 0; x < kDpl; ++x) acc[x] = 0.f;
+        M = -INFINITY;
+        L = 0.f;
+        bad = false;
+      }
+      const float2 ml = slot_ml[s * 8 + gl];
+      bad |= ml.y < 0.f;
+      if (ml.y > 0.f) {
+        const float Mn = fmaxf(M, ml.x);
+        const float sc = exp2f(M - Mn), w = exp2f(ml.x - Mn);
+        L = fmaf(w, ml.y, L * sc);
+        const float2* src = reinterpret_cast<const float2*>(slot_acc + s * rb) + (gl * D + d0) / 2;
+#pragma unroll
+        for (int x = 0; x < kDpl / 2; ++x) {
+          const float2 a = src[x];
+          acc[2 * x] = fmaf(w, a.x, acc[2 * x] * sc);
+          acc[2 * x + 1] = fmaf(w, a.y, acc[2 * x + 1] * sc);
         }
+        M = Mn;
+      }
+      if (++cr == jobs[cj].nrec) {                   // job cj complete: write its output
+        if (active) {
+          const int b = jobs[cj].b, hq = h * G + g;
+          const float Lf = bad ? 0.f : L;
+          const float inv = Lf > 0.f ? 1.f / Lf : 0.f;
+          __half* o = p.out + ((size_t)b * p.Hq + hq) * D + d0;
+#pragma unroll
+          for (int x = 0; x < kDpl; x += 2)
+            *reinterpret_cast<__half2*>(o + x) = __floats2half2_rn(acc[x] * inv, acc[x + 1] * inv);
+          if (sub == 0 && p.lse)
+            p.lse[(size_t)b * p.Hq + hq] = Lf > 0.f ? (M + log2f(Lf)) * 0.69314718055994531f : -INFINITY;
+        }
+        ++cj;
+        cr = 0;
       }
     }
   }
-  for (int off = 1; off < lph; off <<= 1) Ls += __shfl_xor_sync(gmask, Ls, off);
-  if (!active) return;
-  const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-  for (int x = 0; x < kMaxDpl; x += 2)
-    if (x < dpl) *reinterpret_cast<__half2*>(o + x) = __floats2half2_rn(acc[x] * inv, acc[x + 1] * inv);
-  if (sub == 0 && p.lse)
-    p.lse[(size_t)b * p.Hq + hq] = Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
 }
 
-// Called by every consumer warp after it wrote its partial record of (segment b, KV
-// head h): counts the record, and the warp that writes the last of the
-// n_cta(b) * NG records of (b, h) merges them. No warp waits for another.
 template <int D>
-__device__ void finish_segment(const DecodeParams& p, int b, int h, const int* cu, int per) {
+__device__ void merge_run(const DecodeParams& p, int h, const MergeJob* jobs, int nj, const MergeBuf& mb) {
+  if (nj == 0) return;
+  const int G = p.G;
+  if (G <= 1) merge_jobs<D, 1>(p, h, jobs, nj, mb.buf, mb.bytes);
+  else if (G <= 2) merge_jobs<D, 2>(p, h, jobs, nj, mb.buf, mb.bytes);
+  else if (G <= 4) merge_jobs<D, 4>(p, h, jobs, nj, mb.buf, mb.bytes);
+  else merge_jobs<D, 8>(p, h, jobs, nj, mb.buf, mb.bytes);
+}
+
+// True when sequence b has pages outside this CTA's range [start, end).
+__device__ __forceinline__ bool crosses_ctas(const int* cu, int b, int start, int end) {
+  return cu[b] < start || cu[b + 1] > end;
+}
+
+// A warp's completion, after its stream ends (its records all written):
+//  * the sequences that continue in other CTAs (only the first and the last segment of
+//    the range can) take one ticket per warp for (b, h); the warp that takes the last
+//    of the n_cta * NG tickets merges (b, h) and resets the ticket;
+//  * with NG > 1, the sequences wholly inside the range are merged by the NG warps of
+//    head h after a barrier among those warps only, dealt round-robin.
+// Mid-stream segment ends take no fence and no atomic: the tickets of the CTA's first
+// segment are taken here too, which delays nothing, as its last records come from the
+// CTA before, finishing at about the same time.
+template <int D>
+__device__ void finish_warp(const DecodeParams& p, const int* cu, int start, int end, int per, int b_first,
+                            int b_last, int h, int grp, MergeBuf mb) {
   const int lane = threadIdx.x & 31;
-  const int c0 = cu[b] / per;
-  const int n_cta = (cu[b + 1] - 1) / per - c0 + 1;
-  const int expected = n_cta * p.NG;
-  int* ticket = p.plan + kPlanTicket + b * kMaxKvHeads + h;
+  const int NG = p.NG;
+  int cross_b[2] = {-1, -1};
+  int n_cross = 0;
+  if (cu[b_first] != cu[b_first + 1] && crosses_ctas(cu, b_first, start, end)) cross_b[n_cross++] = b_first;
+  if (b_last != b_first && crosses_ctas(cu, b_last, start, end)) cross_b[n_cross++] = b_last;
   __syncwarp();
-  int last = 0;
-  if (lane == 0) {
-    __threadfence();
-    last = (atomicAdd(ticket, 1) == expected - 1) ? 1 : 0;
+  unsigned last_mask = 0;
+  if (lane == 0 && n_cross > 0) {
+    __threadfence();                                   // this warp's records before its tickets
+    int old[2] = {0, 0};
+    int* tk[2] = {nullptr, nullptr};
+    for (int e = 0; e < n_cross; ++e) {
+      tk[e] = p.plan + kPlanTicket + cross_b[e] * kMaxKvHeads + h;
+      old[e] = atomicAdd(tk[e], 1);
+    }
+    for (int e = 0; e < n_cross; ++e) {
+      const int b = cross_b[e];
+      const int c0 = cu[b] / per, n_cta = (cu[b + 1] - 1) / per - c0 + 1;
+      if (old[e] == n_cta * NG - 1) {
+        last_mask |= 1u << e;
+        *tk[e] = 0;
+      }
+    }
+    if (last_mask) __threadfence();                    // other warps' records after their tickets
   }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  int* badp = p.plan + kPlanBad + b * kMaxKvHeads + h;
-  const bool bad = __ldcg(badp) != 0;
-  merge_heads<D>(p, b, h, c0, n_cta, bad);
-  __syncwarp();
-  if (lane == 0) {
-    *ticket = 0;
-    if (bad) *badp = 0;
+  last_mask = __shfl_sync(0xffffffffu, last_mask, 0);
+  constexpr int kMaxJobs = 16;
+  MergeJob jobs[kMaxJobs];
+  int nj = 0;
+  for (int e = 0; e < n_cross; ++e) {
+    if (!(last_mask & (1u << e))) continue;
+    const int b = cross_b[e];
+    const int c0 = cu[b] / per, n_cta = (cu[b + 1] - 1) / per - c0 + 1;
+    jobs[nj++] = MergeJob{b, (b + c0) * NG, n_cta * NG};
   }
+  // sequences wholly inside this CTA (NG > 1 only: with NG = 1 the consumer wrote them
+  // out directly): b_first + 1 .. b_last - 1, plus the ends when they do not cross
+  // (the same set for every warp of the CTA)
+  const int lo = (cu[b_first] == cu[b_first + 1] || crosses_ctas(cu, b_first, start, end)) ? b_first + 1 : b_first;
+  const int hi = crosses_ctas(cu, b_last, start, end) ? b_last - 1 : b_last;
+  if (NG > 1 && lo <= hi) {
+    // the NG warps of head h (warps h, h + Hkv, ...): their records of these sequences
+    // are complete after this barrier (ids 1..4; NG > 1 means Hkv <= 4)
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + h), "r"(32 * NG) : "memory");
+    int item = 0;
+    for (int b = lo; b <= hi; ++b) {
+      if (cu[b] == cu[b + 1]) continue;
+      if (item++ % NG != grp) continue;
+      if (nj == kMaxJobs) {
+        merge_run<D>(p, h, jobs, nj, mb);
+        nj = 0;
+      }
+      jobs[nj++] = MergeJob{b, (b + (int)blockIdx.x) * NG, NG};
+    }
+  }
+  merge_run<D>(p, h, jobs, nj, mb);
 }
 
 }  // namespace ekv
