@@ -30,7 +30,10 @@
  *    scale, a seq_len above the block table's capacity, a demotion page holding
  *    NaN/inf, a timed-out pipeline wait) set a sticky error word in the context; the
  *    affected outputs are zeroed (decode) or left untouched (demote). Read and clear it
- *    with ekv_get_error.
+ *    with ekv_get_error. In decode, a page that fails its check zeroes the output (and
+ *    sets lse = -inf) of the query heads that read it: the whole sequence for a bad
+ *    page id or mode byte, the G query heads of one KV head for a bad per-(page, head)
+ *    scale; a sequence whose seq_len fails is written as empty.
  *  - A context is bound to the device current at ekv_create and to one stream at a
  *    time: calls that overlap on different streams race on its scratch.
  *
