@@ -55,6 +55,34 @@ def test_bad_scale_is_reported(ekv_lib, torch_cuda, bad):
         assert (code, detail) == (ekv_lib.EKV_ERR_DEVICE_CHECK, ekv_lib.EKV_DETAIL_SCALE)
 
 
+@pytest.mark.parametrize("lens", [[40, 70, 20], [700, 33, 1500, 5, 260]])
+def test_bad_scale_zeroes_only_the_heads_of_its_kv_head(ekv_lib, torch_cuda, lens):
+    """A bad per-(page, KV head) scale zeroes the G query heads of that KV head in the
+    sequences that read the page; every other output matches the oracle. The longer
+    length mix splits sequences over many CTAs, so the mark travels through the merge."""
+    case = wl.make_decode_case(lens, 8, 2, 64, v_format="mixed", scale_mode=1, pool_pages=260, seed=43)
+    good_scales = case.v_scales.copy()
+    B, G = len(lens), 4
+    bl = int(np.argmax(case.seq_lens))                     # a compact page of the longest sequence
+    p = next(int(case.block_table[bl, j]) for j in range((case.seq_lens[bl] + 15) // 16)
+             if case.page_mode[case.block_table[bl, j]] == 1)
+    ref_out, ref_lse = oracle_decode(case)                 # with the good scales
+    case.v_scales = good_scales.copy()
+    case.v_scales[p, 1] = float("nan")
+    ctx = ekv_lib.Context(8, 2, 64, B)
+    out, lse = gpu_decode(ctx, to_device(case))
+    assert ctx.error() == (ekv_lib.EKV_ERR_DEVICE_CHECK, ekv_lib.EKV_DETAIL_SCALE)
+    users = [b for b in range(B) if p in set(case.block_table[b, :(case.seq_lens[b] + 15) // 16])]
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    for b in range(B):
+        for hq in range(8):
+            if b in users and hq // G == 1:
+                assert np.all(o[b, hq] == 0) and np.isneginf(l[b, hq]), (b, hq)
+            else:
+                assert np.abs(o[b, hq] - ref_out[b, hq]).max() <= 2e-3, (b, hq)
+                assert abs(l[b, hq] - ref_lse[b, hq]) <= 1e-3, (b, hq)
+
+
 def test_seq_len_above_capacity_is_reported(ekv_lib, torch_cuda):
     case = base_case()
     case.seq_lens = case.seq_lens.copy()
