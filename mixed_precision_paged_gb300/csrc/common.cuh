@@ -107,6 +107,16 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* tm, in
       : "memory");
 }
 
+// 1-D bulk copy global -> shared of `bytes` (multiple of 16; both addresses 16-byte
+// aligned), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared through L2 (cp.async, LSU path), and the
 // wait for all of this thread's such copies.
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
@@ -116,6 +126,12 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Order this thread's generic-proxy reads of shared memory before the TMA (async-proxy)
+// writes that refill it.
+__device__ __forceinline__ void fence_reads_before_refill() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Byte offset inside a 1024-byte-aligned TMA box after the hardware swizzle:

@@ -66,7 +66,8 @@ struct Slot {
   static constexpr int kBytes = kK + kV;
 };
 
-cudaError_t set_smem_attr(const void* kern);
+// Opt a kernel into `bytes` of dynamic shared memory, once per (kernel, device).
+cudaError_t set_smem_attr(const void* kern, int bytes = kSplitSmemMax);
 size_t split_layout(DecodeParams& p, int D, int vmode, int algo);
 
 }  // namespace ekv

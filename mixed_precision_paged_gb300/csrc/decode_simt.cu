@@ -251,8 +251,8 @@ decode_split_simt(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 }
 
 // ------------------------------------------------------------------ launchers
-// Opt the split kernels into large dynamic shared memory, once per (kernel, device).
-cudaError_t set_smem_attr(const void* kern) {
+// Opt a kernel into `bytes` of dynamic shared memory, once per (kernel, device).
+cudaError_t set_smem_attr(const void* kern, int bytes) {
   static std::mutex mu;
   static std::set<std::pair<const void*, int>> done;
   int dev = 0;
@@ -260,7 +260,7 @@ cudaError_t set_smem_attr(const void* kern) {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (done.count({kern, dev})) return cudaSuccess;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmemMax);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) done.insert({kern, dev});
   return e;
 }

@@ -298,7 +298,7 @@ ekv_status ekv_demote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_b
   p.Hkv = Hkv;
   p.D = D;
   p.err = c->err;
-  return launch_demote(p, n, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+  return launch_demote(p, n, c->num_sms, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
 }
 
 ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {

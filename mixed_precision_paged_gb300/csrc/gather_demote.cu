@@ -1,7 +1,8 @@
 // gather_demote.cu -- compact-prefill gather and TARGET -> compact demotion kernels.
 //
-// Both are pure HBM streaming: one CTA per page, 16-byte vector loads issued all
-// before the first use (8 KiB..32 KiB in flight per CTA, several CTAs per SM).
+// Both are pure HBM streaming. Gather: one CTA per page, 16-byte vector loads issued
+// all before the first use. Demotion: two persistent CTAs per SM with a ring of whole
+// pages in shared memory.
 #include "common.cuh"
 #include "gather_demote.cuh"
 
@@ -117,98 +118,169 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
 // Per KV head h: a = max|x|, s = a / 448 (IEEE fp32 divide; 1 when a == 0),
 // code = E4M3_rn_satfinite(x / s). The quotient is the IEEE one, computed by
 // div_by_scale (reciprocal + one Markstein correction; checked against __fdiv_rn).
-// The whole FP16 page is loaded into registers before the first barrier, so the
-// codes may overwrite the page's first half.
-__global__ void __launch_bounds__(256, 4)
-demote_kernel(const DemoteParams p) {
+//
+// Streaming form: 4 CTAs per SM, each takes items blockIdx.x, blockIdx.x + grid, ...
+// of page_ids. A CTA keeps S whole FP16 pages (48 KiB worth: one 32 KiB page for
+// H_kv = 8, D = 128) in flight in a shared-memory ring: one 1-D bulk copy per page,
+// issued by thread 0 as soon as the page before it in that slot is in registers, so
+// the next page streams in while the CTA reduces and requantises. (Measured on 8,192
+// pages: 4 CTAs x 48 KiB 6.3 TB/s, 3 x 64 KiB 6.1, 2 x 96 KiB 5.6, 1 x 192 KiB 4.3:
+// the per-page work, not the depth of the ring, sets the pace, so more CTAs win.) Each thread holds 8 x 16 B of the page in registers, so
+// the codes may overwrite the page's first half in global memory. Page ids and mode
+// bytes of the next kChunk items are staged in shared memory by the whole CTA.
+constexpr int kDemoteThreads = 256;
+constexpr int kDemoteMaxStages = 8;
+constexpr int kDemoteRingBytes = 48 * 1024;
+constexpr int kDemoteChunk = 512;
+
+__global__ void __launch_bounds__(kDemoteThreads, 4)
+demote_kernel(const DemoteParams p, int n, int S) {
   constexpr int kMaxVec = 8;                      // 8 x 16 B x 256 = 32 KiB (H_kv*D <= 1024)
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kDemoteMaxStages];
+  __shared__ int s_stage_page[kDemoteMaxStages];  // page in a slot, -1 = nothing to do
+  __shared__ int s_ids[kDemoteChunk];             // page of an item, -1 = skip it
   __shared__ unsigned int s_amax[kMaxKvHeads];
   __shared__ float s_scale[kMaxKvHeads];
   __shared__ float s_recip[kMaxKvHeads];
   __shared__ int s_nonfinite;
   const int tid = threadIdx.x, lane = tid & 31;
-  const int page = __ldg(p.page_ids + blockIdx.x);
-  if (page < 0 || page >= p.num_pages) {
-    if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, blockIdx.x);
-    return;
+  const int grid = (int)gridDim.x;
+  const int m = (n - (int)blockIdx.x + grid - 1) / grid;   // items of this CTA
+  const int page_bytes = kPage * p.Hkv * p.D * 2;
+  const int nvec = page_bytes / 16;
+  const int lanes_per_row = p.D / 8;              // 8 or 16: a row of one head
+  // Vector v holds elements 8v .. 8v+7 of the page [16][H_kv][D], in KV head
+  // (8v / D) mod H_kv. A thread's vectors are tid + 256u, 2048u elements apart, a
+  // multiple of H_kv * D (<= 1024): they all lie in the same head.
+  const int head = ((tid * 8) / p.D) % p.Hkv;
+
+  // items k0 .. k0 + kChunk - 1 of this CTA: page id if valid and TARGET, else -1
+  auto load_chunk = [&](int k0) {
+    for (int t = tid; t < kDemoteChunk; t += kDemoteThreads) {
+      const int k = k0 + t;
+      int id = -1;
+      if (k < m) {
+        const int i = (int)blockIdx.x + k * grid;
+        const int page = __ldg(p.page_ids + i);
+        if (page < 0 || page >= p.num_pages) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, i);
+        else if (p.page_mode[page] == EKV_MODE_TARGET_FP16) id = page;   // else already compact
+      }
+      s_ids[t] = id;
+    }
+  };
+  // thread 0: slot k % S receives item k
+  auto issue = [&](int k) {
+    const int sl = k % S;
+    const int page = s_ids[k % kDemoteChunk];
+    s_stage_page[sl] = page;
+    if (page < 0) {
+      mbar_arrive(&full[sl]);
+      return;
+    }
+    mbar_arrive_expect_tx(&full[sl], (uint32_t)page_bytes);
+    bulk_load(ring + sl * page_bytes, p.v_pages + (size_t)page * p.v_page_stride, (uint32_t)page_bytes,
+              &full[sl]);
+  };
+
+  if (tid < S) {
+    mbar_init(&full[tid], 1);
+    fence_barrier_init();
   }
-  if (p.page_mode[page] != EKV_MODE_TARGET_FP16) return;      // already compact: skip
   if (tid < kMaxKvHeads) s_amax[tid] = 0u;
   if (tid == 0) s_nonfinite = 0;
+  load_chunk(0);
   __syncthreads();
-  const int n_elem = kPage * p.Hkv * p.D;
-  const int nvec = n_elem / 8;                    // 8 fp16 per uint4
-  const int lanes_per_row = p.D / 8;              // 8 or 16: a row of one head
-  uint8_t* base = p.v_pages + (size_t)page * p.v_page_stride;
-  const uint4* src = reinterpret_cast<const uint4*>(base);
-  uint4 buf[kMaxVec];
+  if (tid == 0)
+    for (int k = 0; k < min(S, m); ++k) issue(k);
+
+  for (int k = 0; k < m; ++k) {
+    const int sl = k % S;
+    const bool ok = mbar_wait(&full[sl], (uint32_t)(k / S) & 1u);
+    const int page = s_stage_page[sl];
+    uint4 buf[kMaxVec];
+    if (ok && page >= 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(ring + sl * page_bytes);
+      // every vector of this thread lies in KV head `head` (see below): reduce locally
+      // first, fp16 magnitudes compared as unsigned 16-bit pairs (NaN/inf >= 0x7c00)
+      unsigned int mx2 = 0u;
 #pragma unroll
-  for (int u = 0; u < kMaxVec; ++u) {
-    const int v = tid + u * 256;
-    if (v < nvec) buf[u] = src[v];
-  }
-#pragma unroll
-  for (int u = 0; u < kMaxVec; ++u) {
-    const int v = tid + u * 256;
-    if (u * 256 >= nvec) break;                   // block-uniform
-    unsigned int mx = 0u;
-    if (v < nvec) {
-      const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        mx = max(mx, w[q] & 0x7fffu);
-        mx = max(mx, (w[q] >> 16) & 0x7fffu);
+      for (int u = 0; u < kMaxVec; ++u) {
+        const int v = tid + u * kDemoteThreads;
+        if (v < nvec) {
+          buf[u] = src[v];
+          mx2 = __vmaxu2(mx2, __vmaxu2(buf[u].x & 0x7fff7fffu, buf[u].y & 0x7fff7fffu));
+          mx2 = __vmaxu2(mx2, __vmaxu2(buf[u].z & 0x7fff7fffu, buf[u].w & 0x7fff7fffu));
+        }
+      }
+      unsigned int mx = max(mx2 & 0xffffu, mx2 >> 16);
+      for (int off = 1; off < lanes_per_row; off <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if ((lane % lanes_per_row) == 0 && tid < nvec) atomicMax(&s_amax[head], mx);
+    }
+    const int kn = k + S;                          // the item that refills this slot
+    if (kn < m && kn % kDemoteChunk == 0) {        // block-uniform
+      __syncthreads();                             // every read of the old chunk is done
+      load_chunk(kn);
+    }
+    // the slot is in registers (or unused): refill it; a timed-out wait ends the CTA
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_TIMEOUT, blockIdx.x);
+        for (int kk = k; kk < min(k + S, m); ++kk)     // this CTA's copies still in flight
+          mbar_wait(&full[kk % S], (uint32_t)(kk / S) & 1u);
+      }
+      return;
+    }
+    if (tid == 0 && kn < m) {
+      fence_reads_before_refill();
+      issue(kn);
+    }
+    if (page < 0) continue;                        // block-uniform
+    if (tid < p.Hkv) {
+      const unsigned int bits = s_amax[tid];
+      s_amax[tid] = 0u;
+      if (bits >= 0x7c00u) {
+        s_nonfinite = 1;
+      } else {
+        const float a = __half2float(__ushort_as_half((unsigned short)bits));
+        const float sc = a == 0.f ? 1.f : __fdiv_rn(a, 448.f);
+        s_scale[tid] = sc;
+        s_recip[tid] = __frcp_rn(sc);
       }
     }
-    // fp16 magnitudes compare as unsigned integers; NaN/inf are >= 0x7c00
-    for (int off = 1; off < lanes_per_row; off <<= 1)
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (v < nvec && (lane % lanes_per_row) == 0) {
-      const int head = ((v * 8) / p.D) % p.Hkv;
-      atomicMax(&s_amax[head], mx);
-    }
-  }
-  __syncthreads();
-  if (tid < p.Hkv) {
-    const unsigned int bits = s_amax[tid];
-    if (bits >= 0x7c00u) {
-      s_nonfinite = 1;
-    } else {
-      const float a = __half2float(__ushort_as_half((unsigned short)bits));
-      const float sc = a == 0.f ? 1.f : __fdiv_rn(a, 448.f);
-      s_scale[tid] = sc;
-      s_recip[tid] = __frcp_rn(sc);
-    }
-  }
-  __syncthreads();
-  if (s_nonfinite) {
-    if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_NONFINITE_PAGE, page);
-    return;
-  }
+    __syncthreads();
+    const bool skip = s_nonfinite != 0;
+    if (!skip) {
+      uint8_t* base = p.v_pages + (size_t)page * p.v_page_stride;
+      const float s = s_scale[head], rs = s_recip[head];
 #pragma unroll
-  for (int u = 0; u < kMaxVec; ++u) {
-    const int v = tid + u * 256;
-    if (v >= nvec) break;
-    const int head = ((v * 8) / p.D) % p.Hkv;
-    const float s = s_scale[head], rs = s_recip[head];
-    const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
-    uint32_t packed[2];
+      for (int u = 0; u < kMaxVec; ++u) {
+        const int v = tid + u * kDemoteThreads;
+        if (v >= nvec) break;
+        const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+        uint32_t packed[2];
 #pragma unroll
-    for (int q = 0; q < 4; q += 2) {
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w[q + 1]));
-      const uint16_t lo = float2_to_e4m3x2(div_by_scale(a.x, s, rs), div_by_scale(a.y, s, rs));
-      const uint16_t hi = float2_to_e4m3x2(div_by_scale(b.x, s, rs), div_by_scale(b.y, s, rs));
-      packed[q / 2] = (uint32_t)lo | ((uint32_t)hi << 16);
+        for (int q = 0; q < 4; q += 2) {
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+          const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w[q + 1]));
+          const uint16_t lo = float2_to_e4m3x2(div_by_scale(a.x, s, rs), div_by_scale(a.y, s, rs));
+          const uint16_t hi = float2_to_e4m3x2(div_by_scale(b.x, s, rs), div_by_scale(b.y, s, rs));
+          packed[q / 2] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+        *reinterpret_cast<uint2*>(base + (size_t)v * 8) = make_uint2(packed[0], packed[1]);
+      }
+      if (tid < p.Hkv) p.scale_out[(size_t)page * p.Hkv + tid] = s_scale[tid];
     }
-    *reinterpret_cast<uint2*>(base + (size_t)v * 8) = make_uint2(packed[0], packed[1]);
+    __syncthreads();                               // s_nonfinite and the scales are read
+    if (tid == 0) {
+      if (skip) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_NONFINITE_PAGE, page);
+      else p.page_mode[page] = EKV_MODE_COMPACT_E4M3;
+      s_nonfinite = 0;
+    }
   }
-  __syncthreads();
-  if (tid < p.Hkv) p.scale_out[(size_t)page * p.Hkv + tid] = s_scale[tid];
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) p.page_mode[page] = EKV_MODE_COMPACT_E4M3;
 }
+
+cudaError_t set_smem_attr(const void* kern, int bytes);
 
 cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int pages, cudaStream_t st) {
   if (pages <= 0) return cudaSuccess;
@@ -216,9 +288,15 @@ cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int page
   return cudaGetLastError();
 }
 
-cudaError_t launch_demote(const DemoteParams& p, int n, cudaStream_t st) {
+cudaError_t launch_demote(const DemoteParams& p, int n, int num_sms, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  demote_kernel<<<n, 256, 0, st>>>(p);
+  const int page_bytes = kPage * p.Hkv * p.D * 2;
+  int S = kDemoteRingBytes / page_bytes;
+  S = S > kDemoteMaxStages ? kDemoteMaxStages : S;
+  const int grid = n < 4 * num_sms ? n : 4 * num_sms;
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(demote_kernel), kDemoteRingBytes);
+  if (e != cudaSuccess) return e;
+  demote_kernel<<<grid, kDemoteThreads, (size_t)S * page_bytes, st>>>(p, n, S);
   return cudaGetLastError();
 }
 

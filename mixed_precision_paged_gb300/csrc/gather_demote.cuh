@@ -46,6 +46,6 @@ struct DemoteParams {
 };
 
 cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int pages, cudaStream_t st);
-cudaError_t launch_demote(const DemoteParams& p, int n, cudaStream_t st);
+cudaError_t launch_demote(const DemoteParams& p, int n, int num_sms, cudaStream_t st);
 
 }  // namespace ekv

@@ -199,11 +199,6 @@ __device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, i
   else tma_load_5d(dst + S::kK, tmV16, 0, 0, 0, h, page, bar);
 }
 
-// Order this warp's generic-proxy reads of a slot before the TMA (async-proxy) writes
-// that refill it.
-__device__ __forceinline__ void fence_reads_before_refill() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Common prologue of the split kernels: plan, this CTA's page range, barriers.
 // Returns false when the CTA has no pages.

@@ -102,6 +102,27 @@ def test_demote_bit_exact(ekv_lib, torch_cuda, hkv, d, std):
     assert np.array_equal(sc[demoted], rs[demoted])
 
 
+@pytest.mark.parametrize("P,n,hkv,d", [(4096, 4000, 8, 128), (160000, 158000, 1, 64)])
+def test_demote_streams_many_pages_per_cta(ekv_lib, torch_cuda, P, n, hkv, d):
+    """Enough pages that every CTA of the persistent demotion kernel cycles its slot
+    ring many times (first case: ~13 pages per CTA through 3 slots), and (second case:
+    more than 512 pages per CTA) restages its page-id table. Some pages are already
+    compact and are skipped."""
+    rng = np.random.default_rng(37)
+    x = (rng.standard_normal((P, 16, hkv, d)) * 2 ** 0.5).astype(np.float16)
+    vb = x.reshape(P, -1).view(np.uint8).copy()
+    mode = np.zeros(P, dtype=np.uint8)
+    mode[rng.choice(P, size=P // 50, replace=False)] = 1
+    ids = rng.permutation(P)[:n]
+    v, m, sc, err = run_demote(ekv_lib, torch_cuda, vb, ids, mode, hkv, d)
+    rv, rm, rs = odm.demote_pages(vb, ids, mode, np.zeros((P, hkv), np.float32), hkv, d)
+    assert err == (0, 0)
+    assert np.array_equal(m, rm)
+    assert np.array_equal(v, rv)
+    demoted = np.array([p for p in ids if mode[p] == 0])
+    assert np.array_equal(sc[demoted], rs[demoted])
+
+
 def test_demote_then_gather_round_trip(ekv_lib, torch_cuda):
     import torch
     rng = np.random.default_rng(33)
