@@ -16,6 +16,9 @@ It is written from the pages' statement of the problem, plainly and slowly:
                 attention").
 * ``gather`` -- compact-prefill gather of K16/V8 pages into an FP16 workspace
                 (knlp.io "What changes in vLLM's prefill routing?").
+* ``base``   -- ElasticKV BASE value pages (FP16 high byte, low byte zero-filled):
+                value, TARGET -> BASE demotion, exact promotion (ElasticKV Sec. 3.2,
+                App. B.2-B.3).
 * ``demote`` -- TARGET -> compact requantisation of FP16 value pages with absmax
                 scales (ElasticKV Sec. 3.4 "Transition protocols", with the compact
                 format of the knlp.io page).
@@ -25,7 +28,7 @@ no code with the CUDA path. Pins that tie each function to something other than
 itself live in ``tests/test_oracle_*.py``.
 """
 
-from . import e4m3, decode, gather, demote  # noqa: F401
+from . import base, e4m3, decode, gather, demote  # noqa: F401
 
 PAGE_SIZE = 16
 MODE_TARGET_FP16 = 0

@@ -20,7 +20,7 @@ import math
 
 import numpy as np
 
-from . import e4m3
+from . import base, e4m3
 
 PAGE_SIZE = 16
 MODE_TARGET_FP16 = 0
@@ -44,6 +44,8 @@ def dequant_value_page(v_page_bytes, mode, scale_row, H_kv, D, S=PAGE_SIZE):
         codes = v_page_bytes[:n].reshape(S, H_kv, D)
         s = np.asarray(scale_row, dtype=np.float64).reshape(1, H_kv, 1)
         return e4m3.decode(codes) * s
+    if mode == base.MODE_BASE:
+        return base.base_value(v_page_bytes[:n]).reshape(S, H_kv, D)
     raise ValueError(f"unknown page mode {mode}")
 
 
@@ -66,8 +68,8 @@ def sequence_kv(b, k_pages, v_pages, v_scales, scale_mode, page_mode, uniform_mo
         p = int(block_table[b][j])
         mode = uniform_mode if page_mode is None else int(page_mode[p])
         ks.append(k_pages[p].astype(np.float64))
-        vs.append(dequant_value_page(v_pages[p], mode,
-                                     _scale_row(v_scales, scale_mode, p, H_kv), H_kv, D, S))
+        srow = _scale_row(v_scales, scale_mode, p, H_kv) if mode == MODE_COMPACT_E4M3 else None
+        vs.append(dequant_value_page(v_pages[p], mode, srow, H_kv, D, S))
     if n_pages == 0:
         return np.zeros((0, H_kv, D)), np.zeros((0, H_kv, D))
     K = np.concatenate(ks, axis=0)[:L]

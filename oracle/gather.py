@@ -20,7 +20,7 @@ Definition used (each step exact or a single IEEE rounding):
 
 import numpy as np
 
-from . import e4m3
+from . import base, e4m3
 
 PAGE_SIZE = 16
 MODE_TARGET_FP16 = 0
@@ -51,6 +51,9 @@ def gather_prefill(k_pages, v_pages, v_scales, scale_mode, page_mode, uniform_mo
         mode = uniform_mode if page_mode is None else int(page_mode[p])
         if mode == MODE_TARGET_FP16:
             ws_v[w] = np.ascontiguousarray(v_pages[p][: 2 * n_elem]).view("<f2").reshape(S, H_kv, D)
+        elif mode == base.MODE_BASE:
+            # ElasticKV BASE: high byte in place, low byte zero (exact, no scale)
+            ws_v[w] = base.base_value(v_pages[p][:n_elem]).astype(np.float16).reshape(S, H_kv, D)
         else:
             vals = e4m3.decode(v_pages[p][:n_elem]).reshape(S, H_kv, D)
             if apply_scale:
