@@ -64,8 +64,15 @@ typedef enum {
   EKV_ERR_DEVICE_CHECK = 5   /* a kernel found bad data (see ekv_get_error detail) */
 } ekv_status;
 
-/* Per-page value fidelity, one uint8 per physical page. */
-typedef enum { EKV_MODE_TARGET_FP16 = 0, EKV_MODE_COMPACT_E4M3 = 1 } ekv_page_mode;
+/* Per-page value fidelity, one uint8 per physical page.
+ *  TARGET_FP16:   the page's value slot holds fp16 [16][H_kv][D].
+ *  COMPACT_E4M3:  its first 16*H_kv*D bytes are E4M3 codes; value = E4M3(code) * scale
+ *                 (knlp.io "Asymmetric K16/V8 KV cache").
+ *  BASE:          its first 16*H_kv*D bytes are the high bytes of the fp16 values; value =
+ *                 the fp16 whose high byte is the stored byte and whose low byte is zero,
+ *                 no scale (ElasticKV Sec. 3.2 and App. B.3: "shift-and-bitcast"). The low
+ *                 bytes, kept by the caller, restore TARGET exactly (ekv_promote_pages). */
+typedef enum { EKV_MODE_TARGET_FP16 = 0, EKV_MODE_COMPACT_E4M3 = 1, EKV_MODE_BASE = 2 } ekv_page_mode;
 
 /* Granularity of the compact-page value scales (fp32, device memory).
  * PER_TENSOR: v_scales[0] applies to every compact page (a per-layer scale is one
@@ -166,6 +173,35 @@ ekv_status ekv_gather_prefill(ekv_ctx* ctx, const void* k_pages, const void* v_p
 ekv_status ekv_demote_pages(ekv_ctx* ctx, void* v_pages, long long v_page_stride_bytes,
                             int num_pages, const int32_t* page_ids, int n,
                             uint8_t* page_mode, float* scale_out, void* stream);
+
+/* TARGET -> BASE demotion, in place (ElasticKV Sec. 3.4 "Transition protocols",
+ * App. B.2). For each page p = page_ids[i] whose page_mode[p] is TARGET: the high
+ * byte of every fp16 value of the page goes to the first 16*H_kv*D bytes of its value
+ * slot (same element order), the low bytes to row i of low_out, then page_mode[p] =
+ * BASE. Pages that are not TARGET are skipped (their row untouched); a page holding
+ * NaN/inf is left TARGET and reported (EKV_DETAIL_NONFINITE_PAGE).
+ *  low_out      bytes [n][16*H_kv*D], 16-byte aligned, or NULL to drop the low bytes
+ *               (the page can then not be promoted exactly). Device memory, or host
+ *               memory the device can address (mapped pinned memory): ElasticKV keeps
+ *               this refinement in CPU backing.
+ * Other arguments as for ekv_demote_pages. */
+ekv_status ekv_demote_pages_base(ekv_ctx* ctx, void* v_pages, long long v_page_stride_bytes,
+                                 int num_pages, const int32_t* page_ids, int n,
+                                 uint8_t* page_mode, void* low_out, void* stream);
+
+/* BASE -> TARGET promotion, in place and exact (ElasticKV App. B.2: one step from the
+ * 8-bit BASE state back to the original 16-bit TARGET). For each page p = page_ids[i]
+ * whose page_mode[p] is BASE: value = (high byte << 8) | low_in[i][e] for every element
+ * e, written as fp16 over the page's value slot, then page_mode[p] = TARGET. Pages
+ * that are not BASE are skipped.
+ *  low_in       bytes [n][16*H_kv*D], 16-byte aligned (the rows ekv_demote_pages_base
+ *               wrote, in the order of this call's page_ids); device or mapped host
+ *               memory.
+ * The new mode is visible in stream order, after the call's work completes; no decode
+ * or gather may read these pages concurrently on another stream. */
+ekv_status ekv_promote_pages(ekv_ctx* ctx, void* v_pages, long long v_page_stride_bytes,
+                             int num_pages, const int32_t* page_ids, int n,
+                             uint8_t* page_mode, const void* low_in, void* stream);
 
 /* Paged decode that allocates nothing, for callers that must not call cudaMalloc on
  * this path (a runtime whose pool owns all device memory, an enqueue hook of a host

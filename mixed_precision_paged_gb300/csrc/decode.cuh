@@ -10,6 +10,8 @@ namespace ekv {
 //   kVFP16  every page TARGET  (page_mode == NULL, uniform TARGET): the native path,
 //           no mode bytes, no scales
 //   kVMixed per-page mode byte, FP16-sized value slots in shared memory
+// Value pool of a launch: all E4M3, all FP16, or per-page modes (TARGET / E4M3 / BASE;
+// also a uniform BASE pool, which has the mixed layout).
 enum VMode { kVE4M3 = 0, kVFP16 = 1, kVMixed = 2 };
 
 // Consumer algorithm: CUDA-core FP32 FMAs or mma.sync tensor-core tiles.
@@ -52,8 +54,9 @@ struct DecodeParams {
   int bar_off, cu_off, pbuf_off;
 };
 
-constexpr int kMetaCompact = 1;
-constexpr int kMetaSkip = 2;
+constexpr int kMetaCompact = 1;   // E4M3 value page
+constexpr int kMetaSkip = 2;      // no page, or a page that failed its checks
+constexpr int kMetaBase = 4;      // BASE value page (FP16 high bytes)
 
 // One ring slot holds one (page, KV head) slice: K [16][D] fp16 as D/64 blocks of 16
 // rows x 128 B (one 5-D TMA box), then V [16][D] as E4M3 rows (one box of 16 x D

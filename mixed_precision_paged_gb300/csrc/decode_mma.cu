@@ -77,6 +77,14 @@ __device__ __forceinline__ uint32_t e4m3_pair_to_h2(uint32_t two_codes) {
   return h2_bits(e4m3x2_to_half2((uint16_t)two_codes));
 }
 
+// The same for a BASE page: each byte is the high byte of an fp16 value whose low
+// byte is zero (ElasticKV App. B.3, shift-and-bitcast): the byte permute alone places
+// V[t][d], V[t+1][d] (and V[t][d+1], V[t+1][d+1]) in the high halves.
+__device__ __forceinline__ void base_rows(uint32_t reg, uint32_t& row_d, uint32_t& row_d1) {
+  row_d = __byte_perm(reg, 0u, 0x2404);    // {0, V[t][d], 0, V[t+1][d]}
+  row_d1 = __byte_perm(reg, 0u, 0x3414);   // {0, V[t][d+1], 0, V[t+1][d+1]}
+}
+
 // A fragment (V^T rows d, cols = tokens) of one m-tile from one ldmatrix.trans
 // register of E4M3 byte pairs: bytes {V[t][d], V[t][d+1], V[t+1][d], V[t+1][d+1]}.
 __device__ __forceinline__ void e4m3_rows(uint32_t reg, uint32_t& row_d, uint32_t& row_d1) {
@@ -108,7 +116,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
   // metadata of the warp's pages, 32 per batch, one per lane: cur = batch of k,
   // nxt = next batch (mode bytes / scales in flight), nxt2 = the one after (ids in flight)
   const float tensor_scale =
-      (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR) ? __ldg(p.v_scales) : 1.f;
+      (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR && p.v_scales) ? __ldg(p.v_scales) : 0.f;
   WarpMeta cur, nxt, nxt2;
   wm_ids(p, cu, start, n_my, grp, lane, cur);
   wm_ids(p, cu, start, n_my, grp, 32 + lane, nxt);
@@ -165,6 +173,8 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
       const int ntok = __shfl_sync(0xffffffffu, cur.ntok, k & 31);
       const float pscale = __shfl_sync(0xffffffffu, cur.scale, k & 31);
       const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (flags & kMetaCompact));
+      const bool base = VMODE == kVMixed && (flags & kMetaBase);
+      const bool bytes8 = compact || base;          // one byte per value: E4M3 or BASE
       const bool skip = (flags & kMetaSkip) != 0;
       seg_bad |= skip;
       const float vs = (compact && !uniform_scale) ? pscale : 1.f;
@@ -181,7 +191,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
           const int kb = s >> 2, c = 2 * (s & 3) + lm_c;
           ldsm_x4(kp + kb * 2048 + swz128(lm_t * 128 + c * 16), kf[s][0], kf[s][1], kf[s][2], kf[s][3]);
         }
-        if (compact) {
+        if (bytes8) {
           const uint32_t vbox = vp;
 #pragma unroll
           for (int j = 0; j < MT / 2; ++j) {
@@ -222,6 +232,10 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
             const uint32_t* rr = vr[i >> 1];
             e4m3_rows(rr[(i & 1) * 2], va[i][0], va[i][1]);
             e4m3_rows(rr[(i & 1) * 2 + 1], va[i][2], va[i][3]);
+          } else if (base) {
+            const uint32_t* rr = vr[i >> 1];
+            base_rows(rr[(i & 1) * 2], va[i][0], va[i][1]);
+            base_rows(rr[(i & 1) * 2 + 1], va[i][2], va[i][3]);
           } else {
             va[i][0] = __byte_perm(vr[i][0], vr[i][1], 0x5410);
             va[i][1] = __byte_perm(vr[i][0], vr[i][1], 0x7632);

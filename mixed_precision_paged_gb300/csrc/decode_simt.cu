@@ -35,7 +35,7 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
   const int n_range = end - start;
   const int n_my = n_range > grp ? (n_range - grp + NG - 1) / NG : 0;
   const float tensor_scale =
-      (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR) ? __ldg(p.v_scales) : 1.f;
+      (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR && p.v_scales) ? __ldg(p.v_scales) : 0.f;
   WarpMeta cur, nxt, nxt2;
   wm_ids(p, cu, start, n_my, grp, lane, cur);
   wm_ids(p, cu, start, n_my, grp, 32 + lane, nxt);
@@ -103,6 +103,7 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
         const uint8_t* vp = kp + S::kK;
         const int ntok = mntok;
         const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (mflags & kMetaCompact));
+        const bool base = VMODE == kVMixed && (mflags & kMetaBase);
         const float vs = compact ? mscale : 1.f;
         float s[4][GP];
 #pragma unroll
@@ -166,6 +167,18 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
                   vp + swz64(t * 64 + lane * 2));
               const float2 a = e4m3x2_to_float2(w2);
               vv[0] = a.x; vv[1 % VPL] = a.y;
+            }
+          } else if (base) {                        // high bytes, low bytes zero
+            if (D == 128) {
+              const uint32_t w4 = *reinterpret_cast<const uint32_t*>(vp + swz128(t * 128 + lane * 4));
+              vv[0] = __half2float(__ushort_as_half((unsigned short)((w4 & 0xffu) << 8)));
+              vv[1] = __half2float(__ushort_as_half((unsigned short)(w4 & 0xff00u)));
+              vv[2 % VPL] = __half2float(__ushort_as_half((unsigned short)((w4 >> 8) & 0xff00u)));
+              vv[3 % VPL] = __half2float(__ushort_as_half((unsigned short)((w4 >> 16) & 0xff00u)));
+            } else {
+              const uint16_t w2 = *reinterpret_cast<const uint16_t*>(vp + swz64(t * 64 + lane * 2));
+              vv[0] = __half2float(__ushort_as_half((unsigned short)((w2 & 0xffu) << 8)));
+              vv[1 % VPL] = __half2float(__ushort_as_half((unsigned short)(w2 & 0xff00u)));
             }
           } else {
             if (D == 128) {

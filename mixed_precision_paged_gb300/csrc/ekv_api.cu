@@ -147,12 +147,12 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
   if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out) return EKV_ERR_INVALID_ARG;
   if (num_pages < 1 || block_table_stride < 1) return EKV_ERR_INVALID_ARG;
   if (scale_mode != EKV_SCALE_PER_TENSOR && scale_mode != EKV_SCALE_PER_PAGE_HEAD) return EKV_ERR_INVALID_ARG;
-  if (uniform_mode != EKV_MODE_TARGET_FP16 && uniform_mode != EKV_MODE_COMPACT_E4M3) return EKV_ERR_INVALID_ARG;
-  const int vmode = page_mode ? kVMixed : (uniform_mode == EKV_MODE_COMPACT_E4M3 ? kVE4M3 : kVFP16);
+  const int vmode = decode_vmode(page_mode, uniform_mode);
+  if (vmode < 0) return EKV_ERR_INVALID_ARG;
   const long long n_elem = (long long)kPage * Hkv * D;
   const long long need = vmode == kVE4M3 ? n_elem : 2 * n_elem;
   if (v_page_stride_bytes < need || (v_page_stride_bytes & 15)) return EKV_ERR_INVALID_ARG;
-  if (vmode != kVFP16 && !v_scales) return EKV_ERR_INVALID_ARG;
+  if (vmode == kVE4M3 && !v_scales) return EKV_ERR_INVALID_ARG;   // mixed: a compact page without scales is a device error
   if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out)) return EKV_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return EKV_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !isfinite(sm_scale)) sm_scale = 1.0f / sqrtf((float)D);
@@ -215,9 +215,9 @@ ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pag
     return EKV_ERR_INVALID_ARG;
   if (num_pages < 1 || block_table_stride < 1 || block_table_rows < 1) return EKV_ERR_INVALID_ARG;
   if (scale_mode != EKV_SCALE_PER_TENSOR && scale_mode != EKV_SCALE_PER_PAGE_HEAD) return EKV_ERR_INVALID_ARG;
-  if (uniform_mode != EKV_MODE_TARGET_FP16 && uniform_mode != EKV_MODE_COMPACT_E4M3) return EKV_ERR_INVALID_ARG;
-  const bool any_compact = page_mode || uniform_mode == EKV_MODE_COMPACT_E4M3;
-  const bool any_target = page_mode || uniform_mode == EKV_MODE_TARGET_FP16;
+  if (uniform_mode < EKV_MODE_TARGET_FP16 || uniform_mode > EKV_MODE_BASE) return EKV_ERR_INVALID_ARG;
+  const bool any_compact = uniform_mode == EKV_MODE_COMPACT_E4M3;   // a mode table: checked per page
+  const bool any_target = page_mode || uniform_mode != EKV_MODE_COMPACT_E4M3;
   const long long n_elem = (long long)kPage * Hkv * D;
   if (v_page_stride_bytes < (any_target ? 2 * n_elem : n_elem) || (v_page_stride_bytes & 15))
     return EKV_ERR_INVALID_ARG;
@@ -275,13 +275,19 @@ ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pag
   return EKV_OK;
 }
 
-ekv_status ekv_demote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_bytes, int num_pages,
-                            const int32_t* page_ids, int n, uint8_t* page_mode, float* scale_out,
-                            void* stream) {
+namespace {
+
+// Shared checks and launch of the page-mode transitions.
+ekv_status transition(ekv_ctx* c, int op, void* v_pages, long long v_page_stride_bytes, int num_pages,
+                      const int32_t* page_ids, int n, uint8_t* page_mode, float* scale_out, uint8_t* low,
+                      void* stream) {
   if (!c || n < 0) return EKV_ERR_INVALID_ARG;
   if (n == 0) return EKV_OK;
   const int Hkv = c->cfg.num_kv_heads, D = c->cfg.head_dim;
-  if (!v_pages || !page_ids || !page_mode || !scale_out || num_pages < 1) return EKV_ERR_INVALID_ARG;
+  if (!v_pages || !page_ids || !page_mode || num_pages < 1) return EKV_ERR_INVALID_ARG;
+  if (op == kToE4M3 && !scale_out) return EKV_ERR_INVALID_ARG;
+  if (op == kPromote && !low) return EKV_ERR_INVALID_ARG;
+  if (low && !aligned16(low)) return EKV_ERR_INVALID_ARG;
   const long long n_elem = (long long)kPage * Hkv * D;
   if (v_page_stride_bytes < 2 * n_elem || (v_page_stride_bytes & 15) || !aligned16(v_pages))
     return EKV_ERR_INVALID_ARG;
@@ -295,10 +301,34 @@ ekv_status ekv_demote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_b
   p.page_ids = page_ids;
   p.page_mode = page_mode;
   p.scale_out = scale_out;
+  p.low = low;
   p.Hkv = Hkv;
   p.D = D;
   p.err = c->err;
-  return launch_demote(p, n, c->num_sms, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+  return launch_transition(p, op, n, c->num_sms, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+}
+
+}  // namespace
+
+ekv_status ekv_demote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_bytes, int num_pages,
+                            const int32_t* page_ids, int n, uint8_t* page_mode, float* scale_out,
+                            void* stream) {
+  return transition(c, kToE4M3, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode, scale_out,
+                    nullptr, stream);
+}
+
+ekv_status ekv_demote_pages_base(ekv_ctx* c, void* v_pages, long long v_page_stride_bytes, int num_pages,
+                                 const int32_t* page_ids, int n, uint8_t* page_mode, void* low_out,
+                                 void* stream) {
+  return transition(c, kToBase, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode, nullptr,
+                    static_cast<uint8_t*>(low_out), stream);
+}
+
+ekv_status ekv_promote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_bytes, int num_pages,
+                             const int32_t* page_ids, int n, uint8_t* page_mode, const void* low_in,
+                             void* stream) {
+  return transition(c, kPromote, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode, nullptr,
+                    static_cast<uint8_t*>(const_cast<void*>(low_in)), stream);
 }
 
 ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {

@@ -1,8 +1,8 @@
 // gather_demote.cu -- compact-prefill gather and TARGET -> compact demotion kernels.
 //
-// Both are pure HBM streaming. Gather: one CTA per page, 16-byte vector loads issued
-// all before the first use. Demotion: two persistent CTAs per SM with a ring of whole
-// pages in shared memory.
+// All are pure HBM streaming. Gather: one CTA per page, 16-byte vector loads issued
+// all before the first use. Mode transitions (demotion to E4M3 or BASE, promotion):
+// four persistent CTAs per SM, each with a ring of whole pages in shared memory.
 #include "common.cuh"
 #include "gather_demote.cuh"
 
@@ -11,8 +11,9 @@ namespace ekv {
 // ------------------------------------------------------------------------ gather
 // knlp.io "What changes in vLLM's prefill routing?": stored K16/V8 pages are copied
 // into one bounded FP16 workspace; V8 is cast to FP16 (quantisation error kept).
-// ws_k[w] = K page (bits); ws_v[w] = TARGET page (bits) or
-// fp16_rn(fp32_rn(E4M3(code) * s)) (fp16(E4M3(code)) when apply_scale == 0).
+// ws_k[w] = K page (bits); ws_v[w] = TARGET page (bits),
+// fp16_rn(fp32_rn(E4M3(code) * s)) (fp16(E4M3(code)) when apply_scale == 0), or for a
+// BASE page the fp16 word (byte << 8) (ElasticKV App. B.3; exact, no scale).
 __global__ void __launch_bounds__(256)
 gather_kernel(const GatherParams p, const GatherRanges r) {
   const int i = blockIdx.x;                       // page index within this launch
@@ -28,14 +29,14 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
   const int tid = threadIdx.x;
   if (tid == 0) p.ws_indices[w] = w;
   int mode = 0;
-  bool bad = page < 0 || page >= p.num_pages;
-  if (!bad) {
+  int detail = (page < 0 || page >= p.num_pages) ? EKV_DETAIL_PAGE_ID : EKV_DETAIL_NONE;
+  if (detail == EKV_DETAIL_NONE) {
     mode = p.page_mode ? (int)__ldg(p.page_mode + page) : p.uniform_mode;
-    if (mode > 1) bad = true;
+    if (mode > EKV_MODE_BASE) detail = EKV_DETAIL_PAGE_MODE;
+    else if (mode == EKV_MODE_COMPACT_E4M3 && p.apply_scale && !p.v_scales) detail = EKV_DETAIL_SCALE;
   }
-  if (bad) {
-    if (tid == 0)
-      report_error(p.err, EKV_ERR_DEVICE_CHECK, mode > 1 ? EKV_DETAIL_PAGE_MODE : EKV_DETAIL_PAGE_ID, w);
+  if (detail != EKV_DETAIL_NONE) {
+    if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, detail, w);
     for (int v = tid; v < nvec16; v += 256) {
       wk[v] = make_uint4(0, 0, 0, 0);
       wv[v] = make_uint4(0, 0, 0, 0);
@@ -74,7 +75,7 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
     }
     return;
   }
-  // compact: 16 codes per uint4, all in one head row (D >= 64)
+  // E4M3 or BASE: 16 bytes per uint4, all in one head row (D >= 64)
   const int nvec8 = n_elem / 16;
   const uint4* sv = reinterpret_cast<const uint4*>(vsrc);
   constexpr int kCodeVecPerThread = 4;            // up to 16 KiB of codes
@@ -83,6 +84,23 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
   for (int u = 0; u < kCodeVecPerThread; ++u) {
     const int v = tid + u * 256;
     if (v < nvec8) buf[u] = __ldg(sv + v);
+  }
+  if (mode == EKV_MODE_BASE) {                     // high byte in place, low byte zero
+#pragma unroll
+    for (int u = 0; u < kCodeVecPerThread; ++u) {
+      const int v = tid + u * 256;
+      if (v >= nvec8) continue;
+      const uint32_t words[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+      uint32_t outw[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        outw[2 * q] = __byte_perm(words[q], 0u, 0x1404);       // {0, b0, 0, b1}
+        outw[2 * q + 1] = __byte_perm(words[q], 0u, 0x3424);   // {0, b2, 0, b3}
+      }
+      wv[2 * v] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+      wv[2 * v + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+    }
+    return;
   }
 #pragma unroll
   for (int u = 0; u < kCodeVecPerThread; ++u) {
@@ -112,29 +130,38 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
   }
 }
 
-// ------------------------------------------------------------------------ demote
-// ElasticKV Sec. 3.4: synchronous in-place demotion; the page reads as compact only
-// after the kernel completes (stream order publishes codes, scales and mode together).
-// Per KV head h: a = max|x|, s = a / 448 (IEEE fp32 divide; 1 when a == 0),
-// code = E4M3_rn_satfinite(x / s). The quotient is the IEEE one, computed by
-// div_by_scale (reciprocal + one Markstein correction; checked against __fdiv_rn).
+// ------------------------------------------------------------------------ transitions
+// ElasticKV Sec. 3.4 "Transition protocols": synchronous, in place; a page reads in its
+// new mode only after the kernel completes (stream order publishes data, scales and
+// mode together).
+//  kToE4M3 (TARGET -> compact): per KV head h, a = max|x|, s = a / 448 (IEEE fp32
+//    divide; 1 when a == 0), code = E4M3_rn_satfinite(x / s). The quotient is the IEEE
+//    one, computed by div_by_scale (reciprocal + one Markstein correction; checked
+//    against __fdiv_rn).
+//  kToBase (TARGET -> BASE, ElasticKV App. B.2): the high bytes of the fp16 values go
+//    to the page's first half, the low bytes to the caller's backing row (if any).
+//  kPromote (BASE -> TARGET, App. B.2): the fp16 words are rebuilt from the page's high
+//    bytes and the backing's low bytes.
+// Demotions skip (and report) a page holding NaN/inf and leave it TARGET.
 //
 // Streaming form: 4 CTAs per SM, each takes items blockIdx.x, blockIdx.x + grid, ...
-// of page_ids. A CTA keeps S whole FP16 pages (48 KiB worth: one 32 KiB page for
-// H_kv = 8, D = 128) in flight in a shared-memory ring: one 1-D bulk copy per page,
-// issued by thread 0 as soon as the page before it in that slot is in registers, so
-// the next page streams in while the CTA reduces and requantises. (Measured on 8,192
-// pages: 4 CTAs x 48 KiB 6.3 TB/s, 3 x 64 KiB 6.1, 2 x 96 KiB 5.6, 1 x 192 KiB 4.3:
-// the per-page work, not the depth of the ring, sets the pace, so more CTAs win.) Each thread holds 8 x 16 B of the page in registers, so
-// the codes may overwrite the page's first half in global memory. Page ids and mode
-// bytes of the next kChunk items are staged in shared memory by the whole CTA.
+// of page_ids. A CTA keeps S stages of 32 KiB worth (the FP16 page; for promotion the
+// high bytes then the low bytes) in flight in a shared-memory ring, filled by 1-D bulk
+// copies that thread 0 issues as soon as the page before it in that slot is in
+// registers, so the next page streams in while the CTA works on this one. (Measured
+// on 8,192 demotions: 4 CTAs x 48 KiB 6.3 TB/s, 3 x 64 KiB 6.1, 2 x 96 KiB 5.6,
+// 1 x 192 KiB 4.3: the per-page work, not the depth of the ring, sets the pace.) Each
+// thread holds its 8 x 16 B of the page in registers, so the page may be rewritten
+// in place. Page ids and mode bytes of the next kChunk items are staged in shared
+// memory by the whole CTA.
 constexpr int kDemoteThreads = 256;
 constexpr int kDemoteMaxStages = 8;
 constexpr int kDemoteRingBytes = 48 * 1024;
 constexpr int kDemoteChunk = 512;
 
+template <int OP>
 __global__ void __launch_bounds__(kDemoteThreads, 4)
-demote_kernel(const DemoteParams p, int n, int S) {
+transition_kernel(const DemoteParams p, int n, int S) {
   constexpr int kMaxVec = 8;                      // 8 x 16 B x 256 = 32 KiB (H_kv*D <= 1024)
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[kDemoteMaxStages];
@@ -147,15 +174,17 @@ demote_kernel(const DemoteParams p, int n, int S) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int grid = (int)gridDim.x;
   const int m = (n - (int)blockIdx.x + grid - 1) / grid;   // items of this CTA
-  const int page_bytes = kPage * p.Hkv * p.D * 2;
-  const int nvec = page_bytes / 16;
+  const int half_bytes = kPage * p.Hkv * p.D;     // one byte per value
+  const int page_bytes = 2 * half_bytes;          // stage size
+  const int nvec = page_bytes / 16;               // fp16 vectors of a page
   const int lanes_per_row = p.D / 8;              // 8 or 16: a row of one head
   // Vector v holds elements 8v .. 8v+7 of the page [16][H_kv][D], in KV head
   // (8v / D) mod H_kv. A thread's vectors are tid + 256u, 2048u elements apart, a
   // multiple of H_kv * D (<= 1024): they all lie in the same head.
   const int head = ((tid * 8) / p.D) % p.Hkv;
+  const int want = OP == kPromote ? EKV_MODE_BASE : EKV_MODE_TARGET_FP16;
 
-  // items k0 .. k0 + kChunk - 1 of this CTA: page id if valid and TARGET, else -1
+  // items k0 .. k0 + kChunk - 1 of this CTA: page id if valid and in the source mode
   auto load_chunk = [&](int k0) {
     for (int t = tid; t < kDemoteChunk; t += kDemoteThreads) {
       const int k = k0 + t;
@@ -164,7 +193,7 @@ demote_kernel(const DemoteParams p, int n, int S) {
         const int i = (int)blockIdx.x + k * grid;
         const int page = __ldg(p.page_ids + i);
         if (page < 0 || page >= p.num_pages) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, i);
-        else if (p.page_mode[page] == EKV_MODE_TARGET_FP16) id = page;   // else already compact
+        else if (p.page_mode[page] == want) id = page;   // else nothing to do
       }
       s_ids[t] = id;
     }
@@ -178,9 +207,15 @@ demote_kernel(const DemoteParams p, int n, int S) {
       mbar_arrive(&full[sl]);
       return;
     }
+    const uint8_t* src = p.v_pages + (size_t)page * p.v_page_stride;
     mbar_arrive_expect_tx(&full[sl], (uint32_t)page_bytes);
-    bulk_load(ring + sl * page_bytes, p.v_pages + (size_t)page * p.v_page_stride, (uint32_t)page_bytes,
-              &full[sl]);
+    if (OP == kPromote) {
+      const size_t i = (size_t)blockIdx.x + (size_t)k * grid;
+      bulk_load(ring + sl * page_bytes, src, (uint32_t)half_bytes, &full[sl]);
+      bulk_load(ring + sl * page_bytes + half_bytes, p.low + i * half_bytes, (uint32_t)half_bytes, &full[sl]);
+    } else {
+      bulk_load(ring + sl * page_bytes, src, (uint32_t)page_bytes, &full[sl]);
+    }
   };
 
   if (tid < S) {
@@ -200,22 +235,37 @@ demote_kernel(const DemoteParams p, int n, int S) {
     const int page = s_stage_page[sl];
     uint4 buf[kMaxVec];
     if (ok && page >= 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(ring + sl * page_bytes);
-      // every vector of this thread lies in KV head `head` (see below): reduce locally
-      // first, fp16 magnitudes compared as unsigned 16-bit pairs (NaN/inf >= 0x7c00)
-      unsigned int mx2 = 0u;
+      if (OP == kPromote) {
+        // fp16 words 8v .. 8v+7 = (high byte << 8) | low byte
+        const uint8_t* st = ring + sl * page_bytes;
 #pragma unroll
-      for (int u = 0; u < kMaxVec; ++u) {
-        const int v = tid + u * kDemoteThreads;
-        if (v < nvec) {
-          buf[u] = src[v];
-          mx2 = __vmaxu2(mx2, __vmaxu2(buf[u].x & 0x7fff7fffu, buf[u].y & 0x7fff7fffu));
-          mx2 = __vmaxu2(mx2, __vmaxu2(buf[u].z & 0x7fff7fffu, buf[u].w & 0x7fff7fffu));
+        for (int u = 0; u < kMaxVec; ++u) {
+          const int v = tid + u * kDemoteThreads;
+          if (v < nvec) {
+            const uint2 hb = *reinterpret_cast<const uint2*>(st + 8 * v);
+            const uint2 lb = *reinterpret_cast<const uint2*>(st + half_bytes + 8 * v);
+            buf[u] = make_uint4(__byte_perm(lb.x, hb.x, 0x5140), __byte_perm(lb.x, hb.x, 0x7362),
+                                __byte_perm(lb.y, hb.y, 0x5140), __byte_perm(lb.y, hb.y, 0x7362));
+          }
         }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(ring + sl * page_bytes);
+        // every vector of this thread lies in KV head `head`: reduce locally first,
+        // fp16 magnitudes compared as unsigned 16-bit pairs (NaN/inf >= 0x7c00)
+        unsigned int mx2 = 0u;
+#pragma unroll
+        for (int u = 0; u < kMaxVec; ++u) {
+          const int v = tid + u * kDemoteThreads;
+          if (v < nvec) {
+            buf[u] = src[v];
+            mx2 = __vmaxu2(mx2, __vmaxu2(buf[u].x & 0x7fff7fffu, buf[u].y & 0x7fff7fffu));
+            mx2 = __vmaxu2(mx2, __vmaxu2(buf[u].z & 0x7fff7fffu, buf[u].w & 0x7fff7fffu));
+          }
+        }
+        unsigned int mx = max(mx2 & 0xffffu, mx2 >> 16);
+        for (int off = 1; off < lanes_per_row; off <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if ((lane % lanes_per_row) == 0 && tid < nvec) atomicMax(&s_amax[head], mx);
       }
-      unsigned int mx = max(mx2 & 0xffffu, mx2 >> 16);
-      for (int off = 1; off < lanes_per_row; off <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      if ((lane % lanes_per_row) == 0 && tid < nvec) atomicMax(&s_amax[head], mx);
     }
     const int kn = k + S;                          // the item that refills this slot
     if (kn < m && kn % kDemoteChunk == 0) {        // block-uniform
@@ -236,12 +286,24 @@ demote_kernel(const DemoteParams p, int n, int S) {
       issue(kn);
     }
     if (page < 0) continue;                        // block-uniform
+    uint8_t* base = p.v_pages + (size_t)page * p.v_page_stride;
+    if (OP == kPromote) {
+      uint4* dst = reinterpret_cast<uint4*>(base);
+#pragma unroll
+      for (int u = 0; u < kMaxVec; ++u) {
+        const int v = tid + u * kDemoteThreads;
+        if (v < nvec) dst[v] = buf[u];
+      }
+      __syncthreads();
+      if (tid == 0) p.page_mode[page] = EKV_MODE_TARGET_FP16;
+      continue;
+    }
     if (tid < p.Hkv) {
       const unsigned int bits = s_amax[tid];
       s_amax[tid] = 0u;
       if (bits >= 0x7c00u) {
         s_nonfinite = 1;
-      } else {
+      } else if (OP == kToE4M3) {
         const float a = __half2float(__ushort_as_half((unsigned short)bits));
         const float sc = a == 0.f ? 1.f : __fdiv_rn(a, 448.f);
         s_scale[tid] = sc;
@@ -250,8 +312,7 @@ demote_kernel(const DemoteParams p, int n, int S) {
     }
     __syncthreads();
     const bool skip = s_nonfinite != 0;
-    if (!skip) {
-      uint8_t* base = p.v_pages + (size_t)page * p.v_page_stride;
+    if (!skip && OP == kToE4M3) {
       const float s = s_scale[head], rs = s_recip[head];
 #pragma unroll
       for (int u = 0; u < kMaxVec; ++u) {
@@ -271,10 +332,24 @@ demote_kernel(const DemoteParams p, int n, int S) {
       }
       if (tid < p.Hkv) p.scale_out[(size_t)page * p.Hkv + tid] = s_scale[tid];
     }
+    if (!skip && OP == kToBase) {
+      uint8_t* low = p.low ? p.low + ((size_t)blockIdx.x + (size_t)k * grid) * half_bytes : nullptr;
+#pragma unroll
+      for (int u = 0; u < kMaxVec; ++u) {
+        const int v = tid + u * kDemoteThreads;
+        if (v >= nvec) break;
+        const uint4 w = buf[u];                    // 8 fp16 words: bytes (low, high) each
+        *reinterpret_cast<uint2*>(base + (size_t)v * 8) =
+            make_uint2(__byte_perm(w.x, w.y, 0x7531), __byte_perm(w.z, w.w, 0x7531));
+        if (low)
+          *reinterpret_cast<uint2*>(low + (size_t)v * 8) =
+              make_uint2(__byte_perm(w.x, w.y, 0x6420), __byte_perm(w.z, w.w, 0x6420));
+      }
+    }
     __syncthreads();                               // s_nonfinite and the scales are read
     if (tid == 0) {
       if (skip) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_NONFINITE_PAGE, page);
-      else p.page_mode[page] = EKV_MODE_COMPACT_E4M3;
+      else p.page_mode[page] = OP == kToBase ? EKV_MODE_BASE : EKV_MODE_COMPACT_E4M3;
       s_nonfinite = 0;
     }
   }
@@ -282,21 +357,29 @@ demote_kernel(const DemoteParams p, int n, int S) {
 
 cudaError_t set_smem_attr(const void* kern, int bytes);
 
-cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int pages, cudaStream_t st) {
-  if (pages <= 0) return cudaSuccess;
-  gather_kernel<<<pages, 256, 0, st>>>(p, r);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_demote(const DemoteParams& p, int n, int num_sms, cudaStream_t st) {
-  if (n <= 0) return cudaSuccess;
+template <int OP>
+static cudaError_t launch_op(const DemoteParams& p, int n, int num_sms, cudaStream_t st) {
   const int page_bytes = kPage * p.Hkv * p.D * 2;
   int S = kDemoteRingBytes / page_bytes;
   S = S > kDemoteMaxStages ? kDemoteMaxStages : S;
   const int grid = n < 4 * num_sms ? n : 4 * num_sms;
-  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(demote_kernel), kDemoteRingBytes);
+  auto kern = transition_kernel<OP>;
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern), kDemoteRingBytes);
   if (e != cudaSuccess) return e;
-  demote_kernel<<<grid, kDemoteThreads, (size_t)S * page_bytes, st>>>(p, n, S);
+  kern<<<grid, kDemoteThreads, (size_t)S * page_bytes, st>>>(p, n, S);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transition(const DemoteParams& p, int op, int n, int num_sms, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (op == kToBase) return launch_op<kToBase>(p, n, num_sms, st);
+  if (op == kPromote) return launch_op<kPromote>(p, n, num_sms, st);
+  return launch_op<kToE4M3>(p, n, num_sms, st);
+}
+
+cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int pages, cudaStream_t st) {
+  if (pages <= 0) return cudaSuccess;
+  gather_kernel<<<pages, 256, 0, st>>>(p, r);
   return cudaGetLastError();
 }
 

@@ -34,18 +34,23 @@ struct GatherParams {
   int* err;
 };
 
+// Page-mode transitions run by the same streaming kernel.
+enum TransitionOp { kToE4M3 = 0, kToBase = 1, kPromote = 2 };
+
 struct DemoteParams {
   uint8_t* v_pages;
   long long v_page_stride;
   int num_pages;
   const int32_t* page_ids;
   uint8_t* page_mode;
-  float* scale_out;
+  float* scale_out;       // kToE4M3: fp32 [num_pages][H_kv]
+  uint8_t* low;           // kToBase: low bytes out [n][16*H_kv*D] (may be null);
+                          // kPromote: low bytes in, same layout
   int Hkv, D;
   int* err;
 };
 
 cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int pages, cudaStream_t st);
-cudaError_t launch_demote(const DemoteParams& p, int n, int num_sms, cudaStream_t st);
+cudaError_t launch_transition(const DemoteParams& p, int op, int n, int num_sms, cudaStream_t st);
 
 }  // namespace ekv

@@ -87,12 +87,12 @@ extern "C" ekv_status ekv_paged_decode_noalloc(int num_q_heads, int num_kv_heads
   if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out) return EKV_ERR_INVALID_ARG;
   if (num_pages < 1 || block_table_stride < 1) return EKV_ERR_INVALID_ARG;
   if (scale_mode != EKV_SCALE_PER_TENSOR && scale_mode != EKV_SCALE_PER_PAGE_HEAD) return EKV_ERR_INVALID_ARG;
-  if (uniform_mode != EKV_MODE_TARGET_FP16 && uniform_mode != EKV_MODE_COMPACT_E4M3) return EKV_ERR_INVALID_ARG;
-  const int vmode = page_mode ? kVMixed : (uniform_mode == EKV_MODE_COMPACT_E4M3 ? kVE4M3 : kVFP16);
+  const int vmode = decode_vmode(page_mode, uniform_mode);
+  if (vmode < 0) return EKV_ERR_INVALID_ARG;
   const long long n_elem = (long long)kPage * Hkv * D;
   if (v_page_stride_bytes < (vmode == kVE4M3 ? n_elem : 2 * n_elem) || (v_page_stride_bytes & 15))
     return EKV_ERR_INVALID_ARG;
-  if (vmode != kVFP16 && !v_scales) return EKV_ERR_INVALID_ARG;
+  if (vmode == kVE4M3 && !v_scales) return EKV_ERR_INVALID_ARG;   // mixed: a compact page without scales is a device error
   if (!is_aligned16(q) || !is_aligned16(k_pages) || !is_aligned16(v_pages) || !is_aligned16(out))
     return EKV_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return EKV_ERR_INVALID_ARG;

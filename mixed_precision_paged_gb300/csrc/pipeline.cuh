@@ -118,7 +118,8 @@ __device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int
   }
 }
 
-// Stage B: checks, mode byte and the KV head's scale of a page whose id is known.
+// Stage B: checks, mode byte (TARGET / E4M3 / BASE) and, for an E4M3 page, the KV
+// head's scale of a page whose id is known. A missing or bad scale skips the page.
 template <int VMODE>
 __device__ __forceinline__ void wm_meta(const DecodeParams& p, float tensor_scale, int h, WarpMeta& m) {
   if (m.b < 0) return;
@@ -128,15 +129,21 @@ __device__ __forceinline__ void wm_meta(const DecodeParams& p, float tensor_scal
     m.flags = kMetaSkip;
     return;
   }
-  const int mode = VMODE == kVE4M3 ? 1 : (VMODE == kVFP16 ? 0 : (int)__ldg(p.page_mode + page));
-  if (mode > 1) {
+  const int mode = VMODE == kVE4M3 ? 1
+                   : (VMODE == kVFP16 ? 0 : (p.page_mode ? (int)__ldg(p.page_mode + page) : p.uniform_mode));
+  if (mode > EKV_MODE_BASE) {
     report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_MODE, b);
     m.flags = kMetaSkip;
     return;
   }
-  if (mode == 0) return;
-  const float s = p.scale_mode == EKV_SCALE_PER_TENSOR ? tensor_scale
-                                                         : __ldg(p.v_scales + (size_t)page * p.Hkv + h);
+  if (mode == EKV_MODE_TARGET_FP16) return;
+  if (mode == EKV_MODE_BASE) {                       // no scale: shift and bitcast
+    m.flags = kMetaBase;
+    return;
+  }
+  const float s = !p.v_scales ? 0.f
+                  : (p.scale_mode == EKV_SCALE_PER_TENSOR ? tensor_scale
+                                                           : __ldg(p.v_scales + (size_t)page * p.Hkv + h));
   if (scale_ok(s)) {
     m.flags = kMetaCompact;
     m.scale = s;
@@ -177,8 +184,8 @@ __device__ __forceinline__ MergeBuf merge_buf(const WarpRing& ring, int slot_byt
 
 // Fill the ring slot of page k (metadata page/flags broadcast by the caller). Lane 0
 // arms the slot's barrier with the slice's bytes and issues one bulk tensor copy per
-// tensor: K through the 5-D fp16 slice map, V through the E4M3 map (compact page) or
-// the fp16 slice map (TARGET page). A skipped page only arrives on the barrier.
+// tensor: K through the 5-D fp16 slice map, V through the byte map (E4M3 or BASE page)
+// or the fp16 slice map (TARGET page). A skipped page only arrives on the barrier.
 template <int D, int VMODE>
 __device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, int page, int flags,
                                            const CUtensorMap* tmK, const CUtensorMap* tmV8,
@@ -191,7 +198,8 @@ __device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, i
     mbar_arrive(bar);
     return;
   }
-  const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (flags & kMetaCompact));
+  // E4M3 and BASE pages both hold one byte per value: the same box
+  const bool compact = VMODE == kVE4M3 || (VMODE == kVMixed && (flags & (kMetaCompact | kMetaBase)));
   uint8_t* dst = ring.slots + (size_t)s * S::kBytes;
   mbar_arrive_expect_tx(bar, S::kK + (compact ? kPage * D : kPage * D * 2));
   tma_load_5d(dst, tmK, 0, 0, 0, h, page, bar);

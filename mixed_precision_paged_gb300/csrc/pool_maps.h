@@ -5,9 +5,9 @@
 //   K and FP16 V: 5-D view (d mod 64, token, d / 64, head, page) of [P][16][H_kv][D]
 //                 fp16; the box {64, 16, D/64, 1, 1} lands as [D/64][16][128 B] with
 //                 the 128B swizzle, i.e. D/64 blocks of 16 rows x 128 B.
-//   E4M3 V:       4-D view (d, head, token, page) of [P][16][H_kv][D] bytes; the box
-//                 {D, 1, 16, 1} lands as [16][D B] (128B swizzle for D = 128, 64B for
-//                 D = 64).
+//   byte V:       4-D view (d, head, token, page) of [P][16][H_kv][D] bytes (E4M3 codes
+//                 or BASE high bytes); the box {D, 1, 16, 1} lands as [16][D B] (128B
+//                 swizzle for D = 128, 64B for D = 64).
 // One instruction per tensor matters: issuing a bulk tensor copy costs the issuing
 // warp the same time whatever the box size, and the consumer warps issue their own.
 #pragma once
@@ -66,6 +66,14 @@ inline bool encode_e4m3_slice_map(CUtensorMap* tm, const void* base, int D, int 
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Value-pool kind of a decode call: per-page modes (a mode table, or a uniform BASE
+// pool, which has the mixed layout), uniform E4M3, or uniform FP16. -1: bad uniform_mode.
+inline int decode_vmode(const uint8_t* page_mode, int uniform_mode) {
+  if (uniform_mode < EKV_MODE_TARGET_FP16 || uniform_mode > EKV_MODE_BASE) return -1;
+  if (page_mode || uniform_mode == EKV_MODE_BASE) return kVMixed;
+  return uniform_mode == EKV_MODE_COMPACT_E4M3 ? kVE4M3 : kVFP16;
 }
 
 // The three maps of one decode call; unused ones stay zeroed. False on an encode error.

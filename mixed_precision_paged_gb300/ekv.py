@@ -31,6 +31,7 @@ EKV_ERR_DEVICE_CHECK = 5
 
 EKV_MODE_TARGET_FP16 = 0
 EKV_MODE_COMPACT_E4M3 = 1
+EKV_MODE_BASE = 2
 EKV_SCALE_PER_TENSOR = 0
 EKV_SCALE_PER_PAGE_HEAD = 1
 
@@ -45,7 +46,7 @@ EKV_DETAIL_PAGE_MODE = 6
 EXPORTED = ["ekv_create", "ekv_destroy", "ekv_paged_decode", "ekv_gather_prefill",
             "ekv_demote_pages", "ekv_get_error", "ekv_profile_enable", "ekv_profile_read",
             "ekv_set_decode_variant", "ekv_query", "ekv_paged_decode_noalloc",
-            "ekv_status_string"]
+            "ekv_demote_pages_base", "ekv_promote_pages", "ekv_status_string"]
 
 
 class ekv_config(ctypes.Structure):
@@ -64,6 +65,8 @@ _lib.ekv_paged_decode.argtypes = [_vp, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i,
 _lib.ekv_gather_prefill.argtypes = [_vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i, _i, _vp,
                                     _i, _vp, _vp, _vp, _i, _i, _vp]
 _lib.ekv_demote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
+_lib.ekv_demote_pages_base.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
+_lib.ekv_promote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
 _lib.ekv_paged_decode_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i,
                                           _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp]
 _lib.ekv_get_error.argtypes = [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]
@@ -165,6 +168,22 @@ def ekv_demote_pages(ctx, v_pages, v_page_stride_bytes, num_pages, page_ids, n, 
     _check(_lib.ekv_demote_pages(ctx, _ptr(v_pages), v_page_stride_bytes, num_pages,
                                  _ptr(page_ids), n, _ptr(page_mode), _ptr(scale_out),
                                  _stream(stream)), "ekv_demote_pages")
+
+
+def ekv_demote_pages_base(ctx, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode,
+                          low_out=None, stream=None):
+    """TARGET -> BASE in place; row i of ``low_out`` receives page_ids[i]'s low bytes."""
+    _check(_lib.ekv_demote_pages_base(ctx, _ptr(v_pages), v_page_stride_bytes, num_pages,
+                                      _ptr(page_ids), n, _ptr(page_mode), _ptr(low_out),
+                                      _stream(stream)), "ekv_demote_pages_base")
+
+
+def ekv_promote_pages(ctx, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode, low_in,
+                      stream=None):
+    """BASE -> TARGET in place from the low bytes ``low_in`` (row i for page_ids[i])."""
+    _check(_lib.ekv_promote_pages(ctx, _ptr(v_pages), v_page_stride_bytes, num_pages,
+                                  _ptr(page_ids), n, _ptr(page_mode), _ptr(low_in),
+                                  _stream(stream)), "ekv_promote_pages")
 
 
 def ekv_get_error(ctx):

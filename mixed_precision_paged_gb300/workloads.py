@@ -25,9 +25,11 @@ import torch
 PAGE_SIZE = 16
 MODE_TARGET_FP16 = 0
 MODE_COMPACT_E4M3 = 1
+MODE_BASE = 2
 SCALE_PER_TENSOR = 0
 SCALE_PER_PAGE_HEAD = 1
 E4M3_NAN = 0x7F
+BASE_NAN = 0x7E             # high byte of the fp16 NaN 0x7E00
 
 
 @dataclass
@@ -74,12 +76,14 @@ def _nan_fp16_bytes(n):
 def make_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_format="e4m3",
                      scale_mode=SCALE_PER_TENSOR, pool_pages=None, seed=0,
                      p_compact=0.5, v_std=1.0, poison=True, q_zero=False,
-                     uniform_v=None, explicit_page_mode=None):
+                     uniform_v=None, explicit_page_mode=None, p_base=0.0):
     """Host-side decode case.
 
     v_format: 'e4m3' (uniform compact pool, stride S*H_kv*D), 'fp16' (uniform TARGET
-    pool, stride S*H_kv*D*2) or 'mixed' (FP16-sized slots, each page TARGET or compact
-    with probability ``p_compact``; ``page_mode`` returned).
+    pool, stride S*H_kv*D*2), 'mixed' (FP16-sized slots, each page compact with
+    probability ``p_compact``, BASE with probability ``p_base``, else TARGET;
+    ``page_mode`` returned) or 'base' (uniform BASE pool with FP16-sized slots).
+    A BASE page holds the high bytes of the FP16 values (ElasticKV's BASE state).
     Pages are placed at a random permutation of a pool of ``pool_pages`` pages.
     """
     rng = np.random.default_rng(seed)
@@ -117,7 +121,10 @@ def make_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_format=
     n_elem = S * H * D
 
     if v_format == "mixed":
-        modes = (rng.random(P) < p_compact).astype(np.uint8)
+        r = rng.random(P)
+        modes = (r < p_compact).astype(np.uint8)
+        if p_base > 0:
+            modes[(r >= p_compact) & (r < p_compact + p_base)] = MODE_BASE
         if explicit_page_mode is not None:
             modes = np.asarray(explicit_page_mode, dtype=np.uint8)
         stride = 2 * n_elem
@@ -126,6 +133,9 @@ def make_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_format=
         stride = n_elem
     elif v_format == "fp16":
         modes = np.full(P, MODE_TARGET_FP16, dtype=np.uint8)
+        stride = 2 * n_elem
+    elif v_format == "base":
+        modes = np.full(P, MODE_BASE, dtype=np.uint8)
         stride = 2 * n_elem
     else:
         raise ValueError(v_format)
@@ -152,6 +162,12 @@ def make_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_format=
             v_pages[p, :n_elem] = c.reshape(-1)
             if stride > n_elem:
                 v_pages[p, n_elem:] = E4M3_NAN if poison else 0
+        elif modes[p] == MODE_BASE:
+            hb = fp16_bytes[p].reshape(S, -1)[:, 1::2].copy()     # high byte of each value
+            if poison:
+                hb[~valid[p]] = BASE_NAN
+            v_pages[p, :n_elem] = hb.reshape(-1)
+            v_pages[p, n_elem:] = BASE_NAN if poison else 0
         else:
             fb = fp16_bytes[p].reshape(S, -1).copy()
             if poison:
@@ -161,7 +177,7 @@ def make_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_format=
         for p in range(P):
             k_pages[p, ~valid[p]] = np.float16(np.nan)
     page_mode = modes if v_format == "mixed" else None
-    uniform_mode = MODE_COMPACT_E4M3 if v_format == "e4m3" else MODE_TARGET_FP16
+    uniform_mode = {"e4m3": MODE_COMPACT_E4M3, "base": MODE_BASE}.get(v_format, MODE_TARGET_FP16)
     return DecodeCase(q=q, k_pages=k_pages, v_pages=v_pages, v_scales=v_scales,
                       scale_mode=scale_mode, page_mode=page_mode, uniform_mode=uniform_mode,
                       block_table=block_table, seq_lens=seq_lens, num_q_heads=num_q_heads,
