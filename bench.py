@@ -46,6 +46,9 @@ WORKLOADS = {
     "mixed_fp16_control": dict(desc="mixed-fidelity batch, all-FP16 control", batch=64, q_heads=32,
                                kv_heads=8, head_dim=128, layers=2, v_format="fp16", scale_mode=0,
                                context="U[512, 32768]"),
+    "mixed_base": dict(desc="mixed-fidelity batch, ElasticKV TARGET/BASE pages", batch=64, q_heads=32,
+                       kv_heads=8, head_dim=128, layers=2, v_format="mixed", scale_mode=1,
+                       context="U[512, 32768]", p_compact=0.0, p_base=0.5),
 }
 
 
@@ -371,7 +374,29 @@ def companions(ekv, torch, peaks):
         if rep >= 3:
             ts.append(s.elapsed_time(e))
     t_d = float(np.median(ts))
-    del flush
+    # BASE: demote the same pages to BASE with a low-byte backing, then promote back
+    low = torch.empty((P // 2, S * H * D), dtype=torch.uint8, device="cuda")
+    tb, tp = [], []
+    for rep in range(8):
+        work.copy_(v16b)
+        mode.zero_()
+        flush.sum()
+        s.record()
+        ekv.ekv_demote_pages_base(ctx.handle, work, work.shape[1], P, ids, P // 2, mode, low)
+        e.record()
+        flush.sum()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record()
+        ekv.ekv_promote_pages(ctx.handle, work, work.shape[1], P, ids, P // 2, mode, low)
+        e2.record()
+        torch.cuda.synchronize()
+        if rep >= 3:
+            tb.append(s.elapsed_time(e))
+            tp.append(s2.elapsed_time(e2))
+    exact = bool(torch.equal(work, v16b))
+    t_b, t_p = float(np.median(tb)), float(np.median(tp))
+    bb = rf.base_transition_bytes(P // 2, H, D)
+    del flush, low
     db = rf.demote_bytes(P // 2, H, D)
     err = ctx.error()
     hbm = peaks["hbm_gbs"]
@@ -380,6 +405,10 @@ def companions(ekv, torch, peaks):
                       "bytes": gb, "what": "16,384 pages in 4 chunks of 4,096 into the FP16 workspace"},
            "demote": {"ms": t_d, "GB/s": db / t_d / 1e6, "frac_of_measured_hbm": db / t_d / 1e6 / hbm,
                       "bytes": db, "what": "8,192 of 16,384 FP16 value pages -> E4M3 + scales"},
+           "demote_base": {"ms": t_b, "GB/s": bb / t_b / 1e6, "frac_of_measured_hbm": bb / t_b / 1e6 / hbm,
+                           "bytes": bb, "what": "the same 8,192 pages -> BASE high bytes + low-byte backing"},
+           "promote": {"ms": t_p, "GB/s": bb / t_p / 1e6, "frac_of_measured_hbm": bb / t_p / 1e6 / hbm,
+                       "bytes": bb, "what": "BASE -> TARGET from the backing", "exact_round_trip": exact},
            "device_error": list(err)}
     ctx.close()
     return out
@@ -428,7 +457,8 @@ def main():
     lens = lens_for(args.workload)
     B, Hq, Hkv, D = len(lens), wk["q_heads"], wk["kv_heads"], wk["head_dim"]
     cases = [wl.device_decode_case(lens, Hq, Hkv, D, v_format=wk["v_format"], scale_mode=wk["scale_mode"],
-                                   seed=args.seed + 7919 * (rank * 1000 + l)) for l in range(layers)]
+                                   seed=args.seed + 7919 * (rank * 1000 + l), p_compact=wk.get("p_compact", 0.5),
+                                   p_base=wk.get("p_base", 0.0)) for l in range(layers)]
     torch.cuda.synchronize()
     # algorithmic bytes per layer call
     per_call = []
@@ -436,7 +466,8 @@ def main():
         if wk["v_format"] == "mixed":
             modes = c.page_mode.cpu().numpy()
             bt = c.block_table.cpu().numpy()
-            vbp = [[1 if modes[bt[b, j]] == 1 else 2 for j in range((l + 15) // 16)] for b, l in enumerate(lens)]
+            code = {0: 2, 1: 1, 2: -1}                  # TARGET, E4M3, BASE (see decode_bytes)
+            vbp = [[code[int(modes[bt[b, j]])] for j in range((l + 15) // 16)] for b, l in enumerate(lens)]
             per_call.append(rf.decode_bytes(lens, Hq, Hkv, D, vbp, per_page_scales=True))
         else:
             per_call.append(rf.decode_bytes(lens, Hq, Hkv, D, 1 if wk["v_format"] == "e4m3" else 2,

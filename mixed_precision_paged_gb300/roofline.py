@@ -36,8 +36,9 @@ def decode_bytes(seq_lens, num_q_heads, num_kv_heads, head_dim, v_bytes_per_page
     seq_lens + scales (4 B per KV head of each compact page in per-page mode, else one
     float) + lse (fp32) when requested. Split-K partials are overhead, not counted.
 
-    ``v_bytes_per_page``: None when every page has the same V element size (then an
-    int, 1 or 2, is passed instead), or a per-sequence list of per-page sizes.
+    ``v_bytes_per_page``: an int (1 or 2) when every page has the same V element size,
+    or a per-sequence list of per-page codes: 2 (TARGET fp16), 1 (E4M3, scaled) or -1
+    (BASE: one byte per value, no scale).
     Returns a dict with 'kv', 'split' (what the split kernel must read) and 'total'.
     """
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
@@ -54,7 +55,7 @@ def decode_bytes(seq_lens, num_q_heads, num_kv_heads, head_dim, v_bytes_per_page
             L = int(seq_lens[b])
             for j, vb in enumerate(v_bytes_per_page[b][: int(pages[b])]):
                 ntok = min(PAGE_SIZE, L - j * PAGE_SIZE)
-                kv += ntok * row * (2 + int(vb))
+                kv += ntok * row * (2 + abs(int(vb)))
                 n_compact += int(vb) == 1
     q = B * num_q_heads * head_dim * 2
     out = B * num_q_heads * head_dim * 2
@@ -82,3 +83,12 @@ def demote_bytes(n_pages, num_kv_heads, head_dim, page_size=PAGE_SIZE):
     read = n_pages * (elem * 2 + 4 + 1)                   # FP16 page, page id, mode
     write = n_pages * (elem + 4 * num_kv_heads + 1)       # codes, scales, mode
     return read + write
+
+
+def base_transition_bytes(n_pages, num_kv_heads, head_dim, page_size=PAGE_SIZE):
+    """Bytes read and written by ``ekv_demote_pages_base`` (with a low-byte backing) or
+    ``ekv_promote_pages`` for ``n_pages`` pages: either way the fp16 page (2 bytes per
+    value) on one side and high + low bytes (1 + 1) on the other, plus id and mode."""
+    elem = page_size * num_kv_heads * head_dim
+    return n_pages * (elem * 2 + elem * 2 + 4 + 2)
+

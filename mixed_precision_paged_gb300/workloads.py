@@ -230,7 +230,7 @@ def gather_demote_shape():
 
 def device_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_format="e4m3",
                        scale_mode=SCALE_PER_TENSOR, seed=0, device="cuda", p_compact=0.5,
-                       pool_slack=0, poison_tail=True):
+                       pool_slack=0, poison_tail=True, p_base=0.0):
     """Same recipe as ``make_decode_case`` drawn on the device (for the full-size
     workloads, whose pools are hundreds of MB to tens of GB). Returns torch tensors."""
     S, H, D = PAGE_SIZE, num_kv_heads, head_dim
@@ -253,7 +253,10 @@ def device_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_forma
     q = torch.randn((B, num_q_heads, D), generator=gen, device=device).to(torch.float16)
     k_pages = torch.randn((P, S, H, D), generator=gen, device=device).to(torch.float16)
     if v_format == "mixed":
-        modes = (torch.rand(P, generator=gen, device=device) < p_compact).to(torch.uint8)
+        r = torch.rand(P, generator=gen, device=device)
+        modes = (r < p_compact).to(torch.uint8)
+        if p_base > 0:
+            modes[(r >= p_compact) & (r < p_compact + p_base)] = MODE_BASE
         stride = 2 * n_elem
     elif v_format == "e4m3":
         modes = torch.ones(P, dtype=torch.uint8, device=device)
@@ -290,6 +293,10 @@ def device_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_forma
             sel = (m == MODE_COMPACT_E4M3)[:, None]
             comp = torch.cat([codes, torch.full_like(codes, E4M3_NAN)], dim=1)
             v_pages[p0:p1] = torch.where(sel, comp, fb)
+            if p_base > 0:                             # BASE: the high bytes, then filler
+                hb = fb[:, 1::2]
+                basep = torch.cat([hb, torch.full_like(hb, BASE_NAN)], dim=1)
+                v_pages[p0:p1] = torch.where((m == MODE_BASE)[:, None], basep, v_pages[p0:p1])
     if poison_tail:
         for b in range(B):
             L = int(lens[b])
@@ -300,6 +307,8 @@ def device_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_forma
                 k_pages[p, r:] = float("nan")
                 if modes[p] == MODE_COMPACT_E4M3:
                     v_pages[p, r * H * D: n_elem] = E4M3_NAN
+                elif modes[p] == MODE_BASE:
+                    v_pages[p, r * H * D: n_elem] = BASE_NAN
                 else:
                     v_pages[p].view(torch.float16)[r * H * D: n_elem] = float("nan")
     v_scales = per_tensor if scale_mode == SCALE_PER_TENSOR else v_scales_pp
