@@ -19,6 +19,8 @@ It is written from the pages' statement of the problem, plainly and slowly:
 * ``base``   -- ElasticKV BASE value pages (FP16 high byte, low byte zero-filled):
                 value, TARGET -> BASE demotion, exact promotion (ElasticKV Sec. 3.2,
                 App. B.2-B.3).
+* ``writer`` -- the K16/V8 cache writer: one new token per sequence into its page row
+                (knlp.io implementation checks: "K bit-exact, V within FP8 noise").
 * ``demote`` -- TARGET -> compact requantisation of FP16 value pages with absmax
                 scales (ElasticKV Sec. 3.4 "Transition protocols", with the compact
                 format of the knlp.io page).
@@ -28,7 +30,7 @@ no code with the CUDA path. Pins that tie each function to something other than
 itself live in ``tests/test_oracle_*.py``.
 """
 
-from . import base, e4m3, decode, gather, demote  # noqa: F401
+from . import base, e4m3, decode, gather, demote, writer  # noqa: F401
 
 PAGE_SIZE = 16
 MODE_TARGET_FP16 = 0
