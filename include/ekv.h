@@ -203,6 +203,28 @@ ekv_status ekv_promote_pages(ekv_ctx* ctx, void* v_pages, long long v_page_strid
                              int num_pages, const int32_t* page_ids, int n,
                              uint8_t* page_mode, const void* low_in, void* stream);
 
+/* K16/V8 cache writer: stores one new token per sequence into the paged cache
+ * (knlp.io "Asymmetric K16/V8 KV cache", implementation checks: "vLLM cache writer: K
+ * bit-exact, V within FP8 noise"). For each b with t = positions[b] >= 0, the token goes
+ * to row t % 16 of page p = block_table[b][t / 16]:
+ *   K row = k_new[b] (fp16 bits);
+ *   V row, by page_mode[p] (or uniform_mode): TARGET = v_new[b] (fp16 bits); COMPACT_E4M3 =
+ *   E4M3_rn_satfinite(fp32_rn(v / s)) with the page's existing scale s (per tensor or
+ *   per (p, KV head)); BASE = the high bytes of v_new[b].
+ * The caller allocates pages and grows seq_lens (to t + 1) itself; the first token of a
+ * page is written into a page whose other rows are not read until later steps fill them.
+ *  k_new, v_new  fp16 [batch][H_kv][D], 16-byte aligned.
+ *  positions     int32 [batch]; < 0 means no token for that sequence this step.
+ * Device checks (reported, nothing written for that sequence): t >= block_table_stride *
+ * 16 (EKV_DETAIL_SEQ_LEN), a page id outside the pool, a mode byte > 2. A compact page
+ * whose scale for a KV head is missing or not positive finite keeps that head's old
+ * bytes (EKV_DETAIL_SCALE). Other arguments as for ekv_paged_decode. */
+ekv_status ekv_append_kv(ekv_ctx* ctx, const void* k_new, const void* v_new, void* k_pages,
+                         void* v_pages, long long v_page_stride_bytes, int num_pages,
+                         const float* v_scales, int scale_mode, const uint8_t* page_mode,
+                         int uniform_mode, const int32_t* block_table, int block_table_stride,
+                         const int32_t* positions, int batch, void* stream);
+
 /* Paged decode that allocates nothing, for callers that must not call cudaMalloc on
  * this path (a runtime whose pool owns all device memory, an enqueue hook of a host
  * framework that forbids allocation, a fixed start-up memory budget). The pages have

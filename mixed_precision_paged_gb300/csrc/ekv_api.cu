@@ -331,6 +331,47 @@ ekv_status ekv_promote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_
                     static_cast<uint8_t*>(const_cast<void*>(low_in)), stream);
 }
 
+ekv_status ekv_append_kv(ekv_ctx* c, const void* k_new, const void* v_new, void* k_pages, void* v_pages,
+                         long long v_page_stride_bytes, int num_pages, const float* v_scales, int scale_mode,
+                         const uint8_t* page_mode, int uniform_mode, const int32_t* block_table,
+                         int block_table_stride, const int32_t* positions, int batch, void* stream) {
+  if (!c || batch < 0) return EKV_ERR_INVALID_ARG;
+  if (batch == 0) return EKV_OK;
+  const int Hkv = c->cfg.num_kv_heads, D = c->cfg.head_dim;
+  if (!k_new || !v_new || !k_pages || !v_pages || !block_table || !positions) return EKV_ERR_INVALID_ARG;
+  if (num_pages < 1 || block_table_stride < 1) return EKV_ERR_INVALID_ARG;
+  if (scale_mode != EKV_SCALE_PER_TENSOR && scale_mode != EKV_SCALE_PER_PAGE_HEAD) return EKV_ERR_INVALID_ARG;
+  const int vmode = decode_vmode(page_mode, uniform_mode);
+  if (vmode < 0) return EKV_ERR_INVALID_ARG;
+  const long long n_elem = (long long)kPage * Hkv * D;
+  if (v_page_stride_bytes < (vmode == kVE4M3 ? n_elem : 2 * n_elem) || (v_page_stride_bytes & 15))
+    return EKV_ERR_INVALID_ARG;
+  if (vmode == kVE4M3 && !v_scales) return EKV_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+    return EKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  c->last_stream = st;
+  AppendParams p;
+  p.k_new = static_cast<const __half*>(k_new);
+  p.v_new = static_cast<const __half*>(v_new);
+  p.k_pages = static_cast<__half*>(k_pages);
+  p.v_pages = static_cast<uint8_t*>(v_pages);
+  p.v_page_stride = v_page_stride_bytes;
+  p.num_pages = num_pages;
+  p.v_scales = v_scales;
+  p.scale_mode = scale_mode;
+  p.page_mode = page_mode;
+  p.uniform_mode = uniform_mode;
+  p.block_table = block_table;
+  p.bt_stride = block_table_stride;
+  p.positions = positions;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.err = c->err;
+  return launch_append(p, batch, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+}
+
 ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {
   if (!c) return EKV_ERR_INVALID_ARG;
   DeviceGuard g(c->device);

@@ -377,6 +377,77 @@ cudaError_t launch_transition(const DemoteParams& p, int op, int n, int num_sms,
   return launch_op<kToE4M3>(p, n, num_sms, st);
 }
 
+// ------------------------------------------------------------------------ writer
+// knlp.io "Asymmetric K16/V8 KV cache" (implementation checks: cache writer "K
+// bit-exact, V within FP8 noise"): the new token t = positions[b] of sequence b goes to
+// row t % 16 of page block_table[b][t / 16]; K as its fp16 bits, V in the page's mode:
+// fp16 bits (TARGET), E4M3_rn_satfinite(x / s) with the page's existing scale (compact;
+// IEEE quotient), or the high bytes (BASE). One CTA per sequence, one 16-byte vector of
+// 8 values per thread. A bad position, page id or mode byte writes nothing; a KV head
+// whose scale is missing or not positive finite keeps its old bytes. All reported.
+__global__ void __launch_bounds__(128)
+append_kernel(const AppendParams p) {
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int t = __ldg(p.positions + b);
+  if (t < 0) return;
+  if (t >= p.bt_stride * kPage) {
+    if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_SEQ_LEN, b);
+    return;
+  }
+  const int page = __ldg(p.block_table + (size_t)b * p.bt_stride + t / kPage);
+  if (page < 0 || page >= p.num_pages) {
+    if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, b);
+    return;
+  }
+  const int mode = p.page_mode ? (int)__ldg(p.page_mode + page) : p.uniform_mode;
+  if (mode > EKV_MODE_BASE) {
+    if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_MODE, b);
+    return;
+  }
+  const int row_elems = p.Hkv * p.D;
+  const int row = t % kPage;
+  const int v = tid;                              // vector of 8 values
+  if (8 * v >= row_elems) return;
+  const uint4 kx = __ldg(reinterpret_cast<const uint4*>(p.k_new + (size_t)b * row_elems) + v);
+  reinterpret_cast<uint4*>(p.k_pages + ((size_t)page * kPage + row) * row_elems)[v] = kx;
+  const uint4 vx = __ldg(reinterpret_cast<const uint4*>(p.v_new + (size_t)b * row_elems) + v);
+  uint8_t* vpage = p.v_pages + (size_t)page * p.v_page_stride;
+  if (mode == EKV_MODE_TARGET_FP16) {
+    reinterpret_cast<uint4*>(vpage + (size_t)row * row_elems * 2)[v] = vx;
+    return;
+  }
+  uint2* dst = reinterpret_cast<uint2*>(vpage + (size_t)row * row_elems) + v;
+  if (mode == EKV_MODE_BASE) {                    // high byte of each fp16 word
+    *dst = make_uint2(__byte_perm(vx.x, vx.y, 0x7531), __byte_perm(vx.z, vx.w, 0x7531));
+    return;
+  }
+  const int head = (8 * v) / p.D;
+  const float s = !p.v_scales ? 0.f
+                  : (p.scale_mode == EKV_SCALE_PER_TENSOR ? __ldg(p.v_scales)
+                                                           : __ldg(p.v_scales + (size_t)page * p.Hkv + head));
+  if (!scale_ok(s)) {
+    report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_SCALE, b);
+    return;
+  }
+  const uint32_t w[4] = {vx.x, vx.y, vx.z, vx.w};
+  uint32_t packed[2];
+#pragma unroll
+  for (int q = 0; q < 4; q += 2) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w[q]));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w[q + 1]));
+    const uint16_t lo = float2_to_e4m3x2(__fdiv_rn(a.x, s), __fdiv_rn(a.y, s));
+    const uint16_t hi = float2_to_e4m3x2(__fdiv_rn(c.x, s), __fdiv_rn(c.y, s));
+    packed[q / 2] = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  *dst = make_uint2(packed[0], packed[1]);
+}
+
+cudaError_t launch_append(const AppendParams& p, int batch, cudaStream_t st) {
+  if (batch <= 0) return cudaSuccess;
+  append_kernel<<<batch, 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int pages, cudaStream_t st) {
   if (pages <= 0) return cudaSuccess;
   gather_kernel<<<pages, 256, 0, st>>>(p, r);

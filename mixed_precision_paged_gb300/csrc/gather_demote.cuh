@@ -50,7 +50,27 @@ struct DemoteParams {
   int* err;
 };
 
+// K16/V8 cache writer: one new token per sequence.
+struct AppendParams {
+  const __half* k_new;      // [B][H_kv][D]
+  const __half* v_new;      // [B][H_kv][D]
+  __half* k_pages;
+  uint8_t* v_pages;
+  long long v_page_stride;
+  int num_pages;
+  const float* v_scales;
+  int scale_mode;
+  const uint8_t* page_mode;
+  int uniform_mode;
+  const int32_t* block_table;
+  int bt_stride;
+  const int32_t* positions; // [B], < 0: no token
+  int Hkv, D;
+  int* err;
+};
+
 cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int pages, cudaStream_t st);
+cudaError_t launch_append(const AppendParams& p, int batch, cudaStream_t st);
 cudaError_t launch_transition(const DemoteParams& p, int op, int n, int num_sms, cudaStream_t st);
 
 }  // namespace ekv

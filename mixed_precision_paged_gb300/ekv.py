@@ -46,7 +46,7 @@ EKV_DETAIL_PAGE_MODE = 6
 EXPORTED = ["ekv_create", "ekv_destroy", "ekv_paged_decode", "ekv_gather_prefill",
             "ekv_demote_pages", "ekv_get_error", "ekv_profile_enable", "ekv_profile_read",
             "ekv_set_decode_variant", "ekv_query", "ekv_paged_decode_noalloc",
-            "ekv_demote_pages_base", "ekv_promote_pages", "ekv_status_string"]
+            "ekv_demote_pages_base", "ekv_promote_pages", "ekv_append_kv", "ekv_status_string"]
 
 
 class ekv_config(ctypes.Structure):
@@ -67,6 +67,7 @@ _lib.ekv_gather_prefill.argtypes = [_vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _v
 _lib.ekv_demote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
 _lib.ekv_demote_pages_base.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
 _lib.ekv_promote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
+_lib.ekv_append_kv.argtypes = [_vp, _vp, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i, _vp, _i, _vp]
 _lib.ekv_paged_decode_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i,
                                           _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp]
 _lib.ekv_get_error.argtypes = [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]
@@ -184,6 +185,16 @@ def ekv_promote_pages(ctx, v_pages, v_page_stride_bytes, num_pages, page_ids, n,
     _check(_lib.ekv_promote_pages(ctx, _ptr(v_pages), v_page_stride_bytes, num_pages,
                                   _ptr(page_ids), n, _ptr(page_mode), _ptr(low_in),
                                   _stream(stream)), "ekv_promote_pages")
+
+
+def ekv_append_kv(ctx, k_new, v_new, k_pages, v_pages, v_page_stride_bytes, num_pages, v_scales,
+                  scale_mode, page_mode, uniform_mode, block_table, block_table_stride, positions, batch,
+                  stream=None):
+    """Write one new token per sequence (positions[b] < 0: none) into the paged cache."""
+    _check(_lib.ekv_append_kv(ctx, _ptr(k_new), _ptr(v_new), _ptr(k_pages), _ptr(v_pages),
+                              v_page_stride_bytes, num_pages, _ptr(v_scales), scale_mode, _ptr(page_mode),
+                              uniform_mode, _ptr(block_table), block_table_stride, _ptr(positions), batch,
+                              _stream(stream)), "ekv_append_kv")
 
 
 def ekv_get_error(ctx):
