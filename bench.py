@@ -394,6 +394,19 @@ def companions(ekv, torch, peaks):
             tb.append(s.elapsed_time(e))
             tp.append(s2.elapsed_time(e2))
     exact = bool(torch.equal(work, v16b))
+    # cache writer: one new token for each of the 32 sequences per call (latency-bound)
+    k_new = torch.randn((32, H, D), generator=g, device="cuda").to(torch.float16)
+    v_new = torch.randn((32, H, D), generator=g, device="cuda").to(torch.float16)
+    pos = torch.full((32,), 512 * 16 - 1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        ekv.ekv_append_kv(ctx.handle, k_new, v_new, k, v8, v8.shape[1], P, sc, 1, None, 1, bt, 512, pos, 32)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(100):
+        ekv.ekv_append_kv(ctx.handle, k_new, v_new, k, v8, v8.shape[1], P, sc, 1, None, 1, bt, 512, pos, 32)
+    e.record()
+    torch.cuda.synchronize()
+    t_a = s.elapsed_time(e) / 100
     t_b, t_p = float(np.median(tb)), float(np.median(tp))
     bb = rf.base_transition_bytes(P // 2, H, D)
     del flush, low
@@ -409,6 +422,9 @@ def companions(ekv, torch, peaks):
                            "bytes": bb, "what": "the same 8,192 pages -> BASE high bytes + low-byte backing"},
            "promote": {"ms": t_p, "GB/s": bb / t_p / 1e6, "frac_of_measured_hbm": bb / t_p / 1e6 / hbm,
                        "bytes": bb, "what": "BASE -> TARGET from the backing", "exact_round_trip": exact},
+           "append": {"us": t_a * 1e3, "GB/s": rf.append_bytes(32, H, D, 1) / t_a / 1e6,
+                      "bytes": rf.append_bytes(32, H, D, 1),
+                      "what": "one token for each of 32 sequences into E4M3 pages (launch-latency bound)"},
            "device_error": list(err)}
     ctx.close()
     return out

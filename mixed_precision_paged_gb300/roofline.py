@@ -92,3 +92,11 @@ def base_transition_bytes(n_pages, num_kv_heads, head_dim, page_size=PAGE_SIZE):
     elem = page_size * num_kv_heads * head_dim
     return n_pages * (elem * 2 + elem * 2 + 4 + 2)
 
+
+def append_bytes(batch, num_kv_heads, head_dim, v_bytes):
+    """Bytes of one ``ekv_append_kv`` call: new K and V read (fp16), the K row written
+    (fp16) and the V row written (``v_bytes`` per value), plus position, block-table
+    entry and (compact) the scale of each sequence."""
+    row = num_kv_heads * head_dim
+    return batch * (row * (2 + 2 + 2 + v_bytes) + 4 + 4 + (4 * num_kv_heads if v_bytes == 1 else 0))
+
