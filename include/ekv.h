@@ -134,6 +134,35 @@ ekv_status ekv_paged_decode(ekv_ctx* ctx, const void* q, const void* k_pages,
                             const int32_t* seq_lens, int batch, float sm_scale,
                             void* out, float* lse, void* stream);
 
+/* Paged decode over ElasticKV's pair-structured value layout (ElasticKV Sec. 3.1 "Pair-
+ * Structured Elastic KV Layout", Sec. 3.2, App. B.3). Same computation as
+ * ekv_paged_decode; the values of logical page p (keys and mode byte stay at p) are
+ * found through a separate value block table, so two compact or BASE pages can share
+ * one physical value slot and free the other for the allocator.
+ *  v_pages        bytes [num_v_slots][v_page_stride_bytes], stride >= 32*H_kv*D: each slot
+ *                 holds one TARGET page or two halves of 16*H_kv*D bytes.
+ *  v_block_table  int32 [batch][block_table_stride]: value location of logical page j of
+ *                 sequence b, a half-slot index e in [0, 2*num_v_slots): a TARGET page fills
+ *                 slot e/2 (e must be even); a compact or BASE page is half e%2 of slot e/2.
+ *  boundaries     int32 [batch][2] or NULL: ElasticKV's structured TARGET-BASE-TARGET
+ *                 layout, pages boundaries[b][0] <= j < boundaries[b][1] of sequence b are
+ *                 BASE and the others TARGET; no mode byte is read. NULL: page_mode (by
+ *                 logical page) or uniform_mode, as in ekv_paged_decode.
+ *  has_base       0: the batch holds TARGET pages only and runs the native FP16 path
+ *                 (ElasticKV's batch-level BASE indicator); modes and boundaries are not
+ *                 read. Nonzero: the elastic path.
+ * A location outside the pool, or an odd one for a TARGET page, is a device error
+ * (EKV_DETAIL_PAGE_ID) that zeroes the heads that read it. Other arguments as for
+ * ekv_paged_decode. */
+ekv_status ekv_paged_decode_elastic(ekv_ctx* ctx, const void* q, const void* k_pages,
+                                    const void* v_pages, long long v_page_stride_bytes,
+                                    int num_pages, int num_v_slots, const float* v_scales,
+                                    int scale_mode, const uint8_t* page_mode, int uniform_mode,
+                                    const int32_t* block_table, const int32_t* v_block_table,
+                                    int block_table_stride, const int32_t* boundaries,
+                                    int has_base, const int32_t* seq_lens, int batch,
+                                    float sm_scale, void* out, float* lse, void* stream);
+
 /* Compact-prefill gather: copies the pages named by `page_range` into consecutive
  * workspace slots, in page_range order.
  *
@@ -202,6 +231,28 @@ ekv_status ekv_demote_pages_base(ekv_ctx* ctx, void* v_pages, long long v_page_s
 ekv_status ekv_promote_pages(ekv_ctx* ctx, void* v_pages, long long v_page_stride_bytes,
                              int num_pages, const int32_t* page_ids, int n,
                              uint8_t* page_mode, const void* low_in, void* stream);
+
+/* Page-mode transitions with value locations (ElasticKV Sec. 3.1 and App. B.2), the
+ * general form of ekv_demote_pages (op 0), ekv_demote_pages_base (op 1) and
+ * ekv_promote_pages (op 2) for the layout of ekv_paged_decode_elastic. Item i concerns
+ * logical page page_ids[i] (its page_mode byte, and for op 0 its scale_out row):
+ *  op 0 / 1     reads the TARGET page at the even location src_loc[i] (its whole slot) and
+ *               writes its E4M3 codes / BASE high bytes to the half at dst_loc[i];
+ *  op 2         reads the BASE half at src_loc[i] and the low bytes low[i], writes the TARGET
+ *               page over the slot of the even location dst_loc[i].
+ * src_loc / dst_loc NULL mean in place (2 * page_ids[i]). Items of one call run
+ * concurrently: no item may write a location another item of the call reads. Packing a
+ * pair (A, B) into A's slot therefore takes two calls: A in place, then B from its slot
+ * to half 1 of A's slot; B's slot is then free.
+ *  low          op 1: bytes [n][16*H_kv*D] out (may be NULL); op 2: in (required).
+ *  num_slots    value slots of v_pages; num_pages: logical pages (page_mode, scale_out).
+ * Skips, checks and errors as for the three calls above; a location outside the pool,
+ * or an odd one where a TARGET page is read or written, is reported (EKV_DETAIL_PAGE_ID)
+ * and its item skipped. */
+ekv_status ekv_transition_pages(ekv_ctx* ctx, int op, void* v_pages, long long v_page_stride_bytes,
+                                int num_slots, int num_pages, const int32_t* page_ids,
+                                const int32_t* src_loc, const int32_t* dst_loc, int n,
+                                uint8_t* page_mode, float* scale_out, void* low, void* stream);
 
 /* K16/V8 cache writer: stores one new token per sequence into the paged cache
  * (knlp.io "Asymmetric K16/V8 KV cache", implementation checks: "vLLM cache writer: K

@@ -52,6 +52,11 @@ struct DecodeParams {
   // shared-memory layout of the launch (set by the host for the slot size and batch)
   int nsl;                  // ring slots per warp
   int bar_off, cu_off, pbuf_off;
+  // elastic layout (ElasticKV Sec. 3.1-3.2), all null / 0 for the plain call:
+  const int32_t* v_block_table;   // [B][bt_stride] value locations (half-slot indices)
+  const int32_t* boundaries;      // [B][2] TARGET-BASE-TARGET boundaries, or null
+  int num_v_slots;                // value slots (locations 0 .. 2*num_v_slots-1)
+  int elastic;                    // 1: values read through v_block_table
 };
 
 constexpr int kMetaCompact = 1;   // E4M3 value page

@@ -42,7 +42,8 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
   wm_meta<VMODE>(p, tensor_scale, h, cur);
   for (int kk = 0; kk < min(ring.nsl, n_my); ++kk)
     ring_issue<D, VMODE>(ring, kk, h, __shfl_sync(0xffffffffu, cur.page, kk),
-                         __shfl_sync(0xffffffffu, cur.flags, kk), tmK, tmV8, tmV16);
+                         __shfl_sync(0xffffffffu, cur.vloc, kk), __shfl_sync(0xffffffffu, cur.flags, kk),
+                         p.elastic != 0, tmK, tmV8, tmV16);
   wm_meta<VMODE>(p, tensor_scale, h, nxt);
   wm_ids(p, cu, start, n_my, grp, 64 + lane, nxt2);
   int k = 0;
@@ -213,7 +214,8 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
         const bool in_cur = (kk >> 5) == (k >> 5);
         const int pg = __shfl_sync(0xffffffffu, in_cur ? cur.page : nxt.page, kk & 31);
         const int fl = __shfl_sync(0xffffffffu, in_cur ? cur.flags : nxt.flags, kk & 31);
-        ring_issue<D, VMODE>(ring, kk, h, pg, fl, tmK, tmV8, tmV16);
+        const int vl = __shfl_sync(0xffffffffu, in_cur ? cur.vloc : nxt.vloc, kk & 31);
+        ring_issue<D, VMODE>(ring, kk, h, pg, vl, fl, p.elastic != 0, tmK, tmV8, tmV16);
       }
     }
     if (timed_out) break;

@@ -133,12 +133,16 @@ ekv_status ekv_set_decode_variant(ekv_ctx* c, int variant) {
   return EKV_OK;
 }
 
-ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, const void* v_pages,
-                            long long v_page_stride_bytes, int num_pages, const float* v_scales,
-                            int scale_mode, const uint8_t* page_mode, int uniform_mode,
-                            const int32_t* block_table, int block_table_stride,
-                            const int32_t* seq_lens, int batch, float sm_scale, void* out,
-                            float* lse, void* stream) {
+namespace {
+
+// Shared body of the plain and the elastic decode. Elastic: v_block_table != null
+// (num_v_slots value slots), boundaries optional, has_base = 0 forces the native path.
+ekv_status decode_impl(ekv_ctx* c, const void* q, const void* k_pages, const void* v_pages,
+                       long long v_page_stride_bytes, int num_pages, int num_v_slots, const float* v_scales,
+                       int scale_mode, const uint8_t* page_mode, int uniform_mode, const int32_t* block_table,
+                       const int32_t* v_block_table, int block_table_stride, const int32_t* boundaries,
+                       int has_base, const int32_t* seq_lens, int batch, float sm_scale, void* out, float* lse,
+                       void* stream) {
   if (!c) return EKV_ERR_INVALID_ARG;
   if (batch < 0) return EKV_ERR_INVALID_ARG;
   if (batch > c->cfg.max_batch) return EKV_ERR_CAPACITY;
@@ -147,8 +151,11 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
   if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !out) return EKV_ERR_INVALID_ARG;
   if (num_pages < 1 || block_table_stride < 1) return EKV_ERR_INVALID_ARG;
   if (scale_mode != EKV_SCALE_PER_TENSOR && scale_mode != EKV_SCALE_PER_PAGE_HEAD) return EKV_ERR_INVALID_ARG;
-  const int vmode = decode_vmode(page_mode, uniform_mode);
+  const bool elastic = v_block_table != nullptr;
+  if (elastic && num_v_slots < 1) return EKV_ERR_INVALID_ARG;
+  int vmode = decode_vmode(page_mode, uniform_mode);
   if (vmode < 0) return EKV_ERR_INVALID_ARG;
+  if (elastic) vmode = has_base ? kVMixed : kVFP16;       // ElasticKV's batch-level indicator
   const long long n_elem = (long long)kPage * Hkv * D;
   const long long need = vmode == kVE4M3 ? n_elem : 2 * n_elem;
   if (v_page_stride_bytes < need || (v_page_stride_bytes & 15)) return EKV_ERR_INVALID_ARG;
@@ -159,10 +166,12 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
 
   DeviceGuard g(c->device);
   CUtensorMap tk, t8, t16;
-  if (!decode_pool_maps(&tk, &t8, &t16, k_pages, v_pages, D, Hkv, num_pages, v_page_stride_bytes, vmode))
+  if (!decode_pool_maps(&tk, &t8, &t16, k_pages, v_pages, D, Hkv, num_pages, v_page_stride_bytes, vmode,
+                        elastic ? num_v_slots : 0))
     return EKV_ERR_INVALID_ARG;
 
   DecodeParams p;
+  memset(&p, 0, sizeof(p));
   p.q = static_cast<const __half*>(q);
   p.block_table = block_table;
   p.seq_lens = seq_lens;
@@ -185,6 +194,10 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
   p.NG = c->NG;
   p.D = D;
   p.qscale = sm_scale * 1.4426950408889634f;
+  p.v_block_table = v_block_table;
+  p.boundaries = elastic ? boundaries : nullptr;
+  p.num_v_slots = elastic ? num_v_slots : num_pages;
+  p.elastic = elastic ? 1 : 0;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   c->last_stream = st;
@@ -200,6 +213,32 @@ ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, cons
     ++c->ev_used;
   }
   return EKV_OK;
+}
+
+}  // namespace
+
+ekv_status ekv_paged_decode(ekv_ctx* c, const void* q, const void* k_pages, const void* v_pages,
+                            long long v_page_stride_bytes, int num_pages, const float* v_scales,
+                            int scale_mode, const uint8_t* page_mode, int uniform_mode,
+                            const int32_t* block_table, int block_table_stride,
+                            const int32_t* seq_lens, int batch, float sm_scale, void* out,
+                            float* lse, void* stream) {
+  return decode_impl(c, q, k_pages, v_pages, v_page_stride_bytes, num_pages, 0, v_scales, scale_mode, page_mode,
+                     uniform_mode, block_table, nullptr, block_table_stride, nullptr, 1, seq_lens, batch, sm_scale,
+                     out, lse, stream);
+}
+
+ekv_status ekv_paged_decode_elastic(ekv_ctx* c, const void* q, const void* k_pages, const void* v_pages,
+                                    long long v_page_stride_bytes, int num_pages, int num_v_slots,
+                                    const float* v_scales, int scale_mode, const uint8_t* page_mode,
+                                    int uniform_mode, const int32_t* block_table, const int32_t* v_block_table,
+                                    int block_table_stride, const int32_t* boundaries, int has_base,
+                                    const int32_t* seq_lens, int batch, float sm_scale, void* out, float* lse,
+                                    void* stream) {
+  if (!v_block_table) return EKV_ERR_INVALID_ARG;
+  return decode_impl(c, q, k_pages, v_pages, v_page_stride_bytes, num_pages, num_v_slots, v_scales, scale_mode,
+                     page_mode, uniform_mode, block_table, v_block_table, block_table_stride, boundaries, has_base,
+                     seq_lens, batch, sm_scale, out, lse, stream);
 }
 
 ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pages,
@@ -279,12 +318,13 @@ namespace {
 
 // Shared checks and launch of the page-mode transitions.
 ekv_status transition(ekv_ctx* c, int op, void* v_pages, long long v_page_stride_bytes, int num_pages,
-                      const int32_t* page_ids, int n, uint8_t* page_mode, float* scale_out, uint8_t* low,
-                      void* stream) {
+                      int num_slots, const int32_t* page_ids, const int32_t* src_loc, const int32_t* dst_loc,
+                      int n, uint8_t* page_mode, float* scale_out, uint8_t* low, void* stream) {
   if (!c || n < 0) return EKV_ERR_INVALID_ARG;
   if (n == 0) return EKV_OK;
   const int Hkv = c->cfg.num_kv_heads, D = c->cfg.head_dim;
-  if (!v_pages || !page_ids || !page_mode || num_pages < 1) return EKV_ERR_INVALID_ARG;
+  if (!v_pages || !page_ids || !page_mode || num_pages < 1 || num_slots < 1) return EKV_ERR_INVALID_ARG;
+  if (op < kToE4M3 || op > kPromote) return EKV_ERR_INVALID_ARG;
   if (op == kToE4M3 && !scale_out) return EKV_ERR_INVALID_ARG;
   if (op == kPromote && !low) return EKV_ERR_INVALID_ARG;
   if (low && !aligned16(low)) return EKV_ERR_INVALID_ARG;
@@ -302,6 +342,9 @@ ekv_status transition(ekv_ctx* c, int op, void* v_pages, long long v_page_stride
   p.page_mode = page_mode;
   p.scale_out = scale_out;
   p.low = low;
+  p.src_loc = src_loc;
+  p.dst_loc = dst_loc;
+  p.num_slots = num_slots;
   p.Hkv = Hkv;
   p.D = D;
   p.err = c->err;
@@ -313,22 +356,30 @@ ekv_status transition(ekv_ctx* c, int op, void* v_pages, long long v_page_stride
 ekv_status ekv_demote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_bytes, int num_pages,
                             const int32_t* page_ids, int n, uint8_t* page_mode, float* scale_out,
                             void* stream) {
-  return transition(c, kToE4M3, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode, scale_out,
-                    nullptr, stream);
+  return transition(c, kToE4M3, v_pages, v_page_stride_bytes, num_pages, num_pages, page_ids, nullptr, nullptr,
+                    n, page_mode, scale_out, nullptr, stream);
 }
 
 ekv_status ekv_demote_pages_base(ekv_ctx* c, void* v_pages, long long v_page_stride_bytes, int num_pages,
                                  const int32_t* page_ids, int n, uint8_t* page_mode, void* low_out,
                                  void* stream) {
-  return transition(c, kToBase, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode, nullptr,
-                    static_cast<uint8_t*>(low_out), stream);
+  return transition(c, kToBase, v_pages, v_page_stride_bytes, num_pages, num_pages, page_ids, nullptr, nullptr,
+                    n, page_mode, nullptr, static_cast<uint8_t*>(low_out), stream);
 }
 
 ekv_status ekv_promote_pages(ekv_ctx* c, void* v_pages, long long v_page_stride_bytes, int num_pages,
                              const int32_t* page_ids, int n, uint8_t* page_mode, const void* low_in,
                              void* stream) {
-  return transition(c, kPromote, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode, nullptr,
-                    static_cast<uint8_t*>(const_cast<void*>(low_in)), stream);
+  return transition(c, kPromote, v_pages, v_page_stride_bytes, num_pages, num_pages, page_ids, nullptr, nullptr,
+                    n, page_mode, nullptr, static_cast<uint8_t*>(const_cast<void*>(low_in)), stream);
+}
+
+ekv_status ekv_transition_pages(ekv_ctx* c, int op, void* v_pages, long long v_page_stride_bytes, int num_slots,
+                                int num_pages, const int32_t* page_ids, const int32_t* src_loc,
+                                const int32_t* dst_loc, int n, uint8_t* page_mode, float* scale_out, void* low,
+                                void* stream) {
+  return transition(c, op, v_pages, v_page_stride_bytes, num_pages, num_slots, page_ids, src_loc, dst_loc, n,
+                    page_mode, scale_out, static_cast<uint8_t*>(low), stream);
 }
 
 ekv_status ekv_append_kv(ekv_ctx* c, const void* k_new, const void* v_new, void* k_pages, void* v_pages,

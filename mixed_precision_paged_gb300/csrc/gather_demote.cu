@@ -157,7 +157,7 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
 constexpr int kDemoteThreads = 256;
 constexpr int kDemoteMaxStages = 8;
 constexpr int kDemoteRingBytes = 48 * 1024;
-constexpr int kDemoteChunk = 512;
+constexpr int kDemoteChunk = 256;   // items staged at a time (small static smem: 4 CTAs per SM)
 
 template <int OP>
 __global__ void __launch_bounds__(kDemoteThreads, 4)
@@ -166,7 +166,10 @@ transition_kernel(const DemoteParams p, int n, int S) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[kDemoteMaxStages];
   __shared__ int s_stage_page[kDemoteMaxStages];  // page in a slot, -1 = nothing to do
+  __shared__ int s_stage_dst[kDemoteMaxStages];   // its destination location
   __shared__ int s_ids[kDemoteChunk];             // page of an item, -1 = skip it
+  __shared__ int s_src[kDemoteChunk];             // its source and destination locations
+  __shared__ int s_dst[kDemoteChunk];
   __shared__ unsigned int s_amax[kMaxKvHeads];
   __shared__ float s_scale[kMaxKvHeads];
   __shared__ float s_recip[kMaxKvHeads];
@@ -184,30 +187,44 @@ transition_kernel(const DemoteParams p, int n, int S) {
   const int head = ((tid * 8) / p.D) % p.Hkv;
   const int want = OP == kPromote ? EKV_MODE_BASE : EKV_MODE_TARGET_FP16;
 
-  // items k0 .. k0 + kChunk - 1 of this CTA: page id if valid and in the source mode
+  // items k0 .. k0 + kChunk - 1 of this CTA: page id if valid and in the source mode,
+  // with its source and destination value locations (half-slot indices)
   auto load_chunk = [&](int k0) {
     for (int t = tid; t < kDemoteChunk; t += kDemoteThreads) {
       const int k = k0 + t;
-      int id = -1;
+      int id = -1, src = 0, dst = 0;
       if (k < m) {
         const int i = (int)blockIdx.x + k * grid;
         const int page = __ldg(p.page_ids + i);
-        if (page < 0 || page >= p.num_pages) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, i);
-        else if (p.page_mode[page] == want) id = page;   // else nothing to do
+        if (page < 0 || page >= p.num_pages) {
+          report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, i);
+        } else if (p.page_mode[page] == want) {   // else nothing to do
+          src = p.src_loc ? __ldg(p.src_loc + i) : 2 * page;
+          dst = p.dst_loc ? __ldg(p.dst_loc + i) : 2 * page;
+          const int full = OP == kPromote ? dst : src;   // the location a TARGET page fills
+          if (src < 0 || dst < 0 || src >= 2 * p.num_slots || dst >= 2 * p.num_slots || (full & 1))
+            report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, i);
+          else
+            id = page;
+        }
       }
       s_ids[t] = id;
+      s_src[t] = src;
+      s_dst[t] = dst;
     }
   };
   // thread 0: slot k % S receives item k
   auto issue = [&](int k) {
     const int sl = k % S;
     const int page = s_ids[k % kDemoteChunk];
+    const int src_loc = s_src[k % kDemoteChunk];
     s_stage_page[sl] = page;
+    s_stage_dst[sl] = s_dst[k % kDemoteChunk];
     if (page < 0) {
       mbar_arrive(&full[sl]);
       return;
     }
-    const uint8_t* src = p.v_pages + (size_t)page * p.v_page_stride;
+    const uint8_t* src = p.v_pages + (size_t)(src_loc >> 1) * p.v_page_stride + (src_loc & 1) * half_bytes;
     mbar_arrive_expect_tx(&full[sl], (uint32_t)page_bytes);
     if (OP == kPromote) {
       const size_t i = (size_t)blockIdx.x + (size_t)k * grid;
@@ -233,6 +250,7 @@ transition_kernel(const DemoteParams p, int n, int S) {
     const int sl = k % S;
     const bool ok = mbar_wait(&full[sl], (uint32_t)(k / S) & 1u);
     const int page = s_stage_page[sl];
+    const int dst_loc = s_stage_dst[sl];
     uint4 buf[kMaxVec];
     if (ok && page >= 0) {
       if (OP == kPromote) {
@@ -286,7 +304,8 @@ transition_kernel(const DemoteParams p, int n, int S) {
       issue(kn);
     }
     if (page < 0) continue;                        // block-uniform
-    uint8_t* base = p.v_pages + (size_t)page * p.v_page_stride;
+    // a demotion writes the half at dst_loc; a promotion the slot of dst_loc (even)
+    uint8_t* base = p.v_pages + (size_t)(dst_loc >> 1) * p.v_page_stride + (dst_loc & 1) * half_bytes;
     if (OP == kPromote) {
       uint4* dst = reinterpret_cast<uint4*>(base);
 #pragma unroll

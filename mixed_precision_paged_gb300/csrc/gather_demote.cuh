@@ -46,6 +46,10 @@ struct DemoteParams {
   float* scale_out;       // kToE4M3: fp32 [num_pages][H_kv]
   uint8_t* low;           // kToBase: low bytes out [n][16*H_kv*D] (may be null);
                           // kPromote: low bytes in, same layout
+  const int32_t* src_loc; // per item, or null (in place): demotions: the TARGET page's
+  const int32_t* dst_loc; // even location; promotion: the BASE half. dst: the half a
+                          // demotion writes / the even location a promotion fills.
+  int num_slots;          // value slots of v_pages (locations 0 .. 2*num_slots-1)
   int Hkv, D;
   int* err;
 };

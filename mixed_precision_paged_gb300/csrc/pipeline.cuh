@@ -92,7 +92,9 @@ __device__ __forceinline__ int plan_pages(const DecodeParams& p, int* cu, int* w
 // ----------------------------------------------------------- per-warp metadata
 // Metadata of the warp's k-th page, one page per lane for 32 consecutive k.
 struct WarpMeta {
-  int page;
+  int page;       // logical page: K rows, mode byte, scales
+  int vloc;       // value coordinate: the page (plain) or its half-slot location (elastic)
+  int lp;         // page index within its sequence
   int ntok;
   int flags;
   int b;
@@ -103,6 +105,8 @@ struct WarpMeta {
 __device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int start, int n_my, int grp, int k,
                                        WarpMeta& m) {
   m.page = 0;
+  m.vloc = 0;
+  m.lp = 0;
   m.ntok = 0;
   m.flags = kMetaSkip;
   m.b = -1;
@@ -112,7 +116,9 @@ __device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int
     const int b = upper_bound_i(cu, p.batch + 1, j) - 1;
     const int lp = j - cu[b];
     m.b = b;
+    m.lp = lp;
     m.page = __ldg(p.block_table + (size_t)b * p.bt_stride + lp);
+    m.vloc = p.elastic ? __ldg(p.v_block_table + (size_t)b * p.bt_stride + lp) : m.page;
     m.ntok = min(kPage, __ldg(p.seq_lens + b) - lp * kPage);
     m.flags = 0;
   }
@@ -129,8 +135,23 @@ __device__ __forceinline__ void wm_meta(const DecodeParams& p, float tensor_scal
     m.flags = kMetaSkip;
     return;
   }
-  const int mode = VMODE == kVE4M3 ? 1
-                   : (VMODE == kVFP16 ? 0 : (p.page_mode ? (int)__ldg(p.page_mode + page) : p.uniform_mode));
+  int mode = VMODE == kVE4M3 ? 1 : (VMODE == kVFP16 ? 0 : p.uniform_mode);
+  if (VMODE == kVMixed) {
+    if (p.boundaries) {                              // TARGET-BASE-TARGET: no mode lookup
+      const int b0 = __ldg(p.boundaries + 2 * b), b1 = __ldg(p.boundaries + 2 * b + 1);
+      mode = (m.lp >= b0 && m.lp < b1) ? EKV_MODE_BASE : EKV_MODE_TARGET_FP16;
+    } else if (p.page_mode) {
+      mode = (int)__ldg(p.page_mode + page);
+    }
+  }
+  if (p.elastic) {                                   // a location inside the value pool,
+    const int v = m.vloc;                            // even for a TARGET page
+    if (v < 0 || v >= 2 * p.num_v_slots || (mode == EKV_MODE_TARGET_FP16 && (v & 1))) {
+      report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, b);
+      m.flags = kMetaSkip;
+      return;
+    }
+  }
   if (mode > EKV_MODE_BASE) {
     report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_MODE, b);
     m.flags = kMetaSkip;
@@ -187,8 +208,8 @@ __device__ __forceinline__ MergeBuf merge_buf(const WarpRing& ring, int slot_byt
 // tensor: K through the 5-D fp16 slice map, V through the byte map (E4M3 or BASE page)
 // or the fp16 slice map (TARGET page). A skipped page only arrives on the barrier.
 template <int D, int VMODE>
-__device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, int page, int flags,
-                                           const CUtensorMap* tmK, const CUtensorMap* tmV8,
+__device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, int page, int vloc, int flags,
+                                           bool elastic, const CUtensorMap* tmK, const CUtensorMap* tmV8,
                                            const CUtensorMap* tmV16) {
   using S = Slot<D, VMODE>;
   if ((threadIdx.x & 31) != 0) return;
@@ -203,8 +224,13 @@ __device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, i
   uint8_t* dst = ring.slots + (size_t)s * S::kBytes;
   mbar_arrive_expect_tx(bar, S::kK + (compact ? kPage * D : kPage * D * 2));
   tma_load_5d(dst, tmK, 0, 0, 0, h, page, bar);
-  if (compact) tma_load_4d(dst + S::kK, tmV8, 0, h, 0, page, bar);
-  else tma_load_5d(dst + S::kK, tmV16, 0, 0, 0, h, page, bar);
+  if (elastic) {                                     // vloc = half-slot location
+    if (compact) tma_load_5d(dst + S::kK, tmV8, 0, h, 0, vloc & 1, vloc >> 1, bar);
+    else tma_load_5d(dst + S::kK, tmV16, 0, 0, 0, h, vloc >> 1, bar);
+  } else {                                           // vloc = page
+    if (compact) tma_load_4d(dst + S::kK, tmV8, 0, h, 0, vloc, bar);
+    else tma_load_5d(dst + S::kK, tmV16, 0, 0, 0, h, vloc, bar);
+  }
 }
 
 

@@ -46,7 +46,8 @@ EKV_DETAIL_PAGE_MODE = 6
 EXPORTED = ["ekv_create", "ekv_destroy", "ekv_paged_decode", "ekv_gather_prefill",
             "ekv_demote_pages", "ekv_get_error", "ekv_profile_enable", "ekv_profile_read",
             "ekv_set_decode_variant", "ekv_query", "ekv_paged_decode_noalloc",
-            "ekv_demote_pages_base", "ekv_promote_pages", "ekv_append_kv", "ekv_status_string"]
+            "ekv_demote_pages_base", "ekv_promote_pages", "ekv_append_kv", "ekv_paged_decode_elastic",
+            "ekv_transition_pages", "ekv_status_string"]
 
 
 class ekv_config(ctypes.Structure):
@@ -67,6 +68,9 @@ _lib.ekv_gather_prefill.argtypes = [_vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _v
 _lib.ekv_demote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
 _lib.ekv_demote_pages_base.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
 _lib.ekv_promote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
+_lib.ekv_paged_decode_elastic.argtypes = [_vp, _vp, _vp, _vp, _ll, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _i, _vp,
+                                          _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp]
+_lib.ekv_transition_pages.argtypes = [_vp, _i, _vp, _ll, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp]
 _lib.ekv_append_kv.argtypes = [_vp, _vp, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i, _vp, _i, _vp]
 _lib.ekv_paged_decode_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i,
                                           _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp]
@@ -185,6 +189,27 @@ def ekv_promote_pages(ctx, v_pages, v_page_stride_bytes, num_pages, page_ids, n,
     _check(_lib.ekv_promote_pages(ctx, _ptr(v_pages), v_page_stride_bytes, num_pages,
                                   _ptr(page_ids), n, _ptr(page_mode), _ptr(low_in),
                                   _stream(stream)), "ekv_promote_pages")
+
+
+def ekv_paged_decode_elastic(ctx, q, k_pages, v_pages, v_page_stride_bytes, num_pages, num_v_slots, v_scales,
+                             scale_mode, page_mode, uniform_mode, block_table, v_block_table,
+                             block_table_stride, boundaries, has_base, seq_lens, batch, sm_scale, out,
+                             lse=None, stream=None):
+    """Decode over the pair-structured value layout (values located through v_block_table)."""
+    _check(_lib.ekv_paged_decode_elastic(ctx, _ptr(q), _ptr(k_pages), _ptr(v_pages), v_page_stride_bytes,
+                                         num_pages, num_v_slots, _ptr(v_scales), scale_mode, _ptr(page_mode),
+                                         uniform_mode, _ptr(block_table), _ptr(v_block_table),
+                                         block_table_stride, _ptr(boundaries), int(has_base), _ptr(seq_lens),
+                                         batch, float(sm_scale), _ptr(out), _ptr(lse), _stream(stream)),
+           "ekv_paged_decode_elastic")
+
+
+def ekv_transition_pages(ctx, op, v_pages, v_page_stride_bytes, num_slots, num_pages, page_ids, src_loc,
+                         dst_loc, n, page_mode, scale_out=None, low=None, stream=None):
+    """Located mode transition: op 0 -> E4M3, 1 -> BASE, 2 promote (see include/ekv.h)."""
+    _check(_lib.ekv_transition_pages(ctx, op, _ptr(v_pages), v_page_stride_bytes, num_slots, num_pages,
+                                     _ptr(page_ids), _ptr(src_loc), _ptr(dst_loc), n, _ptr(page_mode),
+                                     _ptr(scale_out), _ptr(low), _stream(stream)), "ekv_transition_pages")
 
 
 def ekv_append_kv(ctx, k_new, v_new, k_pages, v_pages, v_page_stride_bytes, num_pages, v_scales,

@@ -106,7 +106,7 @@ def test_demote_bit_exact(ekv_lib, torch_cuda, hkv, d, std):
 def test_demote_streams_many_pages_per_cta(ekv_lib, torch_cuda, P, n, hkv, d):
     """Enough pages that every CTA of the persistent demotion kernel cycles its slot
     ring many times (first case: ~13 pages per CTA through 3 slots), and (second case:
-    more than 512 pages per CTA) restages its page-id table. Some pages are already
+    more than 256 pages per CTA) restages its page-id table. Some pages are already
     compact and are skipped."""
     rng = np.random.default_rng(37)
     x = (rng.standard_normal((P, 16, hkv, d)) * 2 ** 0.5).astype(np.float16)
