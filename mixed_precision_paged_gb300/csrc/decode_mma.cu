@@ -93,7 +93,7 @@ __device__ __forceinline__ void e4m3_rows(uint32_t reg, uint32_t& row_d, uint32_
   row_d1 = e4m3_pair_to_h2(x >> 16);
 }
 
-template <int D, int VMODE>
+template <int D, int VMODE, int EL>
 __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV8,
                             const CUtensorMap* tmV16, uint8_t* smem, int start, int end, int b_first,
                             int b_last, int per) {
@@ -118,18 +118,19 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
   const float tensor_scale =
       (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR && p.v_scales) ? __ldg(p.v_scales) : 0.f;
   WarpMeta cur, nxt, nxt2;
-  wm_ids(p, cu, start, n_my, grp, lane, cur);
-  wm_ids(p, cu, start, n_my, grp, 32 + lane, nxt);
-  wm_meta<VMODE>(p, tensor_scale, h, cur);
+  wm_ids<EL>(p, cu, start, n_my, grp, lane, cur);
+  wm_ids<EL>(p, cu, start, n_my, grp, 32 + lane, nxt);
+  wm_meta<VMODE, EL>(p, tensor_scale, h, cur);
   {
     const int n0 = min(ring.nsl, n_my);              // prime the ring
     for (int kk = 0; kk < n0; ++kk)
       ring_issue<D, VMODE>(ring, kk, h, __shfl_sync(0xffffffffu, cur.page, kk),
-                           __shfl_sync(0xffffffffu, cur.vloc, kk), __shfl_sync(0xffffffffu, cur.flags, kk),
-                           p.elastic != 0, tmK, tmV8, tmV16);
+                           EL == kElYes ? __shfl_sync(0xffffffffu, cur.vloc, kk) : __shfl_sync(0xffffffffu, cur.page, kk),
+                           __shfl_sync(0xffffffffu, cur.flags, kk),
+                           EL == kElYes, tmK, tmV8, tmV16);
   }
-  wm_meta<VMODE>(p, tensor_scale, h, nxt);
-  wm_ids(p, cu, start, n_my, grp, 64 + lane, nxt2);
+  wm_meta<VMODE, EL>(p, tensor_scale, h, nxt);
+  wm_ids<EL>(p, cu, start, n_my, grp, 64 + lane, nxt2);
   int k = 0;                                        // next page of this warp
   bool timed_out = false;
 
@@ -158,8 +159,8 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
       if ((k & 31) == 0 && k > 0) {                 // next metadata batch
         cur = nxt;
         nxt = nxt2;
-        wm_meta<VMODE>(p, tensor_scale, h, nxt);
-        wm_ids(p, cu, start, n_my, grp, k + 64 + lane, nxt2);
+        wm_meta<VMODE, EL>(p, tensor_scale, h, nxt);
+        wm_ids<EL>(p, cu, start, n_my, grp, k + 64 + lane, nxt2);
       }
       const int s_idx = k % ring.nsl;
       if (!mbar_wait(&ring.full[s_idx], (uint32_t)(k / ring.nsl) & 1u)) {
@@ -254,8 +255,8 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
           const bool in_cur = (kk >> 5) == (k >> 5);
           const int pg = __shfl_sync(0xffffffffu, in_cur ? cur.page : nxt.page, kk & 31);
           const int fl = __shfl_sync(0xffffffffu, in_cur ? cur.flags : nxt.flags, kk & 31);
-          const int vl = __shfl_sync(0xffffffffu, in_cur ? cur.vloc : nxt.vloc, kk & 31);
-          ring_issue<D, VMODE>(ring, kk, h, pg, vl, fl, p.elastic != 0, tmK, tmV8, tmV16);
+          const int vl = EL == kElYes ? __shfl_sync(0xffffffffu, in_cur ? cur.vloc : nxt.vloc, kk & 31) : pg;
+          ring_issue<D, VMODE>(ring, kk, h, pg, vl, fl, EL == kElYes, tmK, tmV8, tmV16);
         }
       }
       if (!skip) {
@@ -370,7 +371,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
   finish_warp<D>(p, cu, start, end, per, b_first, b_last, h, grp, merge_buf(ring, S::kBytes));
 }
 
-template <int D, int VMODE>
+template <int D, int VMODE, int EL>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_split_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV8,
                  const __grid_constant__ CUtensorMap tmV16, const DecodeParams p) {
@@ -384,29 +385,35 @@ decode_split_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (VMODE != kVFP16) tma_prefetch_desc(&tmV8);
     if (VMODE != kVE4M3) tma_prefetch_desc(&tmV16);
   }
-  consume_mma<D, VMODE>(p, &tmK, &tmV8, &tmV16, smem, start, end, b_first, b_last, per);
+  consume_mma<D, VMODE, EL>(p, &tmK, &tmV8, &tmV16, smem, start, end, b_first, b_last, per);
 }
 
-template <int D, int VMODE>
+template <int D, int VMODE, int EL>
 static cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
                               const DecodeParams& p, int grid, size_t smem, cudaStream_t st) {
-  auto kern = decode_split_mma<D, VMODE>;
+  auto kern = decode_split_mma<D, VMODE, EL>;
   cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, st>>>(tk, t8, t16, p);
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_mma_d(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
+                                const DecodeParams& p, int vmode, int grid, size_t smem, cudaStream_t st) {
+  if (p.elastic) {              // the elastic layout: the native FP16 path or the mixed one
+    if (vmode == kVFP16) return launch_mma<D, kVFP16, kElYes>(tk, t8, t16, p, grid, smem, st);
+    return launch_mma<D, kVMixed, kElYes>(tk, t8, t16, p, grid, smem, st);
+  }
+  if (vmode == kVE4M3) return launch_mma<D, kVE4M3, kElNo>(tk, t8, t16, p, grid, smem, st);
+  if (vmode == kVFP16) return launch_mma<D, kVFP16, kElNo>(tk, t8, t16, p, grid, smem, st);
+  return launch_mma<D, kVMixed, kElNo>(tk, t8, t16, p, grid, smem, st);
+}
+
 cudaError_t launch_split_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
                              const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st) {
-  if (D == 128) {
-    if (vmode == kVE4M3) return launch_mma<128, kVE4M3>(tk, t8, t16, p, grid, smem, st);
-    if (vmode == kVFP16) return launch_mma<128, kVFP16>(tk, t8, t16, p, grid, smem, st);
-    return launch_mma<128, kVMixed>(tk, t8, t16, p, grid, smem, st);
-  }
-  if (vmode == kVE4M3) return launch_mma<64, kVE4M3>(tk, t8, t16, p, grid, smem, st);
-  if (vmode == kVFP16) return launch_mma<64, kVFP16>(tk, t8, t16, p, grid, smem, st);
-  return launch_mma<64, kVMixed>(tk, t8, t16, p, grid, smem, st);
+  return D == 128 ? launch_mma_d<128>(tk, t8, t16, p, vmode, grid, smem, st)
+                  : launch_mma_d<64>(tk, t8, t16, p, vmode, grid, smem, st);
 }
 
 }  // namespace ekv

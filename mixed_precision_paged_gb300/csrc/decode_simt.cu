@@ -37,15 +37,15 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
   const float tensor_scale =
       (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR && p.v_scales) ? __ldg(p.v_scales) : 0.f;
   WarpMeta cur, nxt, nxt2;
-  wm_ids(p, cu, start, n_my, grp, lane, cur);
-  wm_ids(p, cu, start, n_my, grp, 32 + lane, nxt);
-  wm_meta<VMODE>(p, tensor_scale, h, cur);
+  wm_ids<kElRuntime>(p, cu, start, n_my, grp, lane, cur);
+  wm_ids<kElRuntime>(p, cu, start, n_my, grp, 32 + lane, nxt);
+  wm_meta<VMODE, kElRuntime>(p, tensor_scale, h, cur);
   for (int kk = 0; kk < min(ring.nsl, n_my); ++kk)
     ring_issue<D, VMODE>(ring, kk, h, __shfl_sync(0xffffffffu, cur.page, kk),
                          __shfl_sync(0xffffffffu, cur.vloc, kk), __shfl_sync(0xffffffffu, cur.flags, kk),
                          p.elastic != 0, tmK, tmV8, tmV16);
-  wm_meta<VMODE>(p, tensor_scale, h, nxt);
-  wm_ids(p, cu, start, n_my, grp, 64 + lane, nxt2);
+  wm_meta<VMODE, kElRuntime>(p, tensor_scale, h, nxt);
+  wm_ids<kElRuntime>(p, cu, start, n_my, grp, 64 + lane, nxt2);
   int k = 0;
   bool timed_out = false;
 
@@ -84,8 +84,8 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
       if ((k & 31) == 0 && k > 0) {
         cur = nxt;
         nxt = nxt2;
-        wm_meta<VMODE>(p, tensor_scale, h, nxt);
-        wm_ids(p, cu, start, n_my, grp, k + 64 + lane, nxt2);
+        wm_meta<VMODE, kElRuntime>(p, tensor_scale, h, nxt);
+        wm_ids<kElRuntime>(p, cu, start, n_my, grp, k + 64 + lane, nxt2);
       }
       const int s_idx = k % ring.nsl;
       if (!mbar_wait(&ring.full[s_idx], (uint32_t)(k / ring.nsl) & 1u)) {

@@ -91,6 +91,15 @@ __device__ __forceinline__ int plan_pages(const DecodeParams& p, int* cu, int* w
 
 // ----------------------------------------------------------- per-warp metadata
 // Metadata of the warp's k-th page, one page per lane for 32 consecutive k.
+// Elastic-layout handling of the per-warp metadata and ring fills, fixed at compile
+// time for the tensor-core consumer (the plain kernels carry none of it) or read from
+// the launch parameters (CUDA-core consumer).
+enum ElasticMode { kElNo = 0, kElYes = 1, kElRuntime = 2 };
+template <int EL>
+__device__ __forceinline__ bool is_elastic(const DecodeParams& p) {
+  return EL == kElYes || (EL == kElRuntime && p.elastic != 0);
+}
+
 struct WarpMeta {
   int page;       // logical page: K rows, mode byte, scales
   int vloc;       // value coordinate: the page (plain) or its half-slot location (elastic)
@@ -102,6 +111,7 @@ struct WarpMeta {
 };
 
 // Stage A: block-table entry of the warp's page k (consumed a batch later).
+template <int EL>
 __device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int start, int n_my, int grp, int k,
                                        WarpMeta& m) {
   m.page = 0;
@@ -118,7 +128,7 @@ __device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int
     m.b = b;
     m.lp = lp;
     m.page = __ldg(p.block_table + (size_t)b * p.bt_stride + lp);
-    m.vloc = p.elastic ? __ldg(p.v_block_table + (size_t)b * p.bt_stride + lp) : m.page;
+    m.vloc = is_elastic<EL>(p) ? __ldg(p.v_block_table + (size_t)b * p.bt_stride + lp) : m.page;
     m.ntok = min(kPage, __ldg(p.seq_lens + b) - lp * kPage);
     m.flags = 0;
   }
@@ -126,7 +136,7 @@ __device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int
 
 // Stage B: checks, mode byte (TARGET / E4M3 / BASE) and, for an E4M3 page, the KV
 // head's scale of a page whose id is known. A missing or bad scale skips the page.
-template <int VMODE>
+template <int VMODE, int EL>
 __device__ __forceinline__ void wm_meta(const DecodeParams& p, float tensor_scale, int h, WarpMeta& m) {
   if (m.b < 0) return;
   const int b = m.b, page = m.page;
@@ -137,14 +147,14 @@ __device__ __forceinline__ void wm_meta(const DecodeParams& p, float tensor_scal
   }
   int mode = VMODE == kVE4M3 ? 1 : (VMODE == kVFP16 ? 0 : p.uniform_mode);
   if (VMODE == kVMixed) {
-    if (p.boundaries) {                              // TARGET-BASE-TARGET: no mode lookup
+    if (is_elastic<EL>(p) && p.boundaries) {         // TARGET-BASE-TARGET: no mode lookup
       const int b0 = __ldg(p.boundaries + 2 * b), b1 = __ldg(p.boundaries + 2 * b + 1);
       mode = (m.lp >= b0 && m.lp < b1) ? EKV_MODE_BASE : EKV_MODE_TARGET_FP16;
     } else if (p.page_mode) {
       mode = (int)__ldg(p.page_mode + page);
     }
   }
-  if (p.elastic) {                                   // a location inside the value pool,
+  if (is_elastic<EL>(p)) {                           // a location inside the value pool,
     const int v = m.vloc;                            // even for a TARGET page
     if (v < 0 || v >= 2 * p.num_v_slots || (mode == EKV_MODE_TARGET_FP16 && (v & 1))) {
       report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, b);
