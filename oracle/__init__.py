@@ -22,6 +22,8 @@ It is written from the pages' statement of the problem, plainly and slowly:
 * ``elastic`` -- ElasticKV's pair-structured value layout (value locations as half
                 slots, a separate value block table), TARGET-BASE-TARGET boundaries, the
                 batch-level BASE indicator and located transitions (Sec. 3.1-3.2, App. B).
+* ``prefill`` -- FP16 causal prefill of whole prompts over the gathered workspace
+                 (knlp.io "What changes in vLLM's prefill routing?": native FP16 prefill).
 * ``writer`` -- the K16/V8 cache writer: one new token per sequence into its page row
                 (knlp.io implementation checks: "K bit-exact, V within FP8 noise").
 * ``demote`` -- TARGET -> compact requantisation of FP16 value pages with absmax
@@ -33,7 +35,7 @@ no code with the CUDA path. Pins that tie each function to something other than
 itself live in ``tests/test_oracle_*.py``.
 """
 
-from . import base, e4m3, decode, gather, demote, writer, elastic  # noqa: F401
+from . import base, e4m3, decode, gather, demote, writer, elastic, prefill  # noqa: F401
 
 PAGE_SIZE = 16
 MODE_TARGET_FP16 = 0
