@@ -186,6 +186,25 @@ ekv_status ekv_gather_prefill(ekv_ctx* ctx, const void* k_pages, const void* v_p
                               void* ws_k, void* ws_v, int32_t* ws_indices, int ws_pages,
                               int apply_scale, void* stream);
 
+/* FP16 causal prefill of whole prompts over the gathered workspace (knlp.io "What
+ * changes in vLLM's prefill routing?": after the gather casts the stored K16/V8 pages into
+ * the bounded FP16 workspace, a native FP16 prefill runs over it; causal, no cached
+ * prefix, no sliding window). For prompt i with len_i = cu_seqlens[i+1] - cu_seqlens[i]
+ * tokens, query position s (row cu_seqlens[i] + s of q) and query head h_q:
+ *   out = sum_{t <= s} softmax_t(sm_scale * q . k_t) v_t,  k_t / v_t = row t % 16 of
+ *   workspace page page_off[i] + t / 16, KV head h_q / G;  lse = log sum e^(...).
+ *  q, out       fp16 [T][H_q][D], T = cu_seqlens[n]; 16-byte aligned.
+ *  ws_k, ws_v   fp16 [ws_pages][16][H_kv][D] (the gather's workspace), 16-byte aligned.
+ *  cu_seqlens   DEVICE int32 [n + 1], nondecreasing; page_off DEVICE int32 [n].
+ *  max_len      HOST int >= every len_i (sizes the grid); a longer prompt is reported
+ *               (EKV_DETAIL_SEQ_LEN) and its later rows are not written.
+ *  lse          fp32 [T][H_q] (natural log) or NULL.
+ * A prompt whose pages fall outside [0, ws_pages) is reported (EKV_DETAIL_PAGE_ID). */
+ekv_status ekv_prefill_attention(ekv_ctx* ctx, const void* q, const void* ws_k, const void* ws_v,
+                                 int ws_pages, const int32_t* cu_seqlens, const int32_t* page_off,
+                                 int n, int max_len, float sm_scale, void* out, float* lse,
+                                 void* stream);
+
 /* TARGET -> compact demotion, in place. For each page p = page_ids[i] whose
  * page_mode[p] is TARGET, and each KV head h:
  *   a = max |x| over the page's 16 x D fp16 values of head h,

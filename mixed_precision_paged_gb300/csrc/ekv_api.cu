@@ -17,6 +17,19 @@ cudaError_t launch_split_simt(const CUtensorMap& tk, const CUtensorMap& t8, cons
                               const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_split_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
                              const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st);
+struct PrefillParams {
+  const __half* q;
+  const __half* ws_k;
+  const __half* ws_v;
+  const int32_t* cu_seqlens;
+  const int32_t* page_off;
+  __half* out;
+  float* lse;
+  int n, Hq, Hkv, G, num_ws_pages;
+  float qscale;
+  int* err;
+};
+cudaError_t launch_prefill(const PrefillParams& p, int D, int max_len, cudaStream_t st);
 }  // namespace ekv
 
 using namespace ekv;
@@ -421,6 +434,38 @@ ekv_status ekv_append_kv(ekv_ctx* c, const void* k_new, const void* v_new, void*
   p.D = D;
   p.err = c->err;
   return launch_append(p, batch, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+}
+
+ekv_status ekv_prefill_attention(ekv_ctx* c, const void* q, const void* ws_k, const void* ws_v, int ws_pages,
+                                 const int32_t* cu_seqlens, const int32_t* page_off, int n, int max_len,
+                                 float sm_scale, void* out, float* lse, void* stream) {
+  if (!c || n < 0 || max_len < 0) return EKV_ERR_INVALID_ARG;
+  if (n == 0 || max_len == 0) return EKV_OK;
+  if (!q || !ws_k || !ws_v || !cu_seqlens || !page_off || !out || ws_pages < 1) return EKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(ws_k) || !aligned16(ws_v) || !aligned16(out)) return EKV_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return EKV_ERR_INVALID_ARG;
+  if (n > 65535) return EKV_ERR_UNSUPPORTED;
+  const int Hq = c->cfg.num_q_heads, Hkv = c->cfg.num_kv_heads, D = c->cfg.head_dim;
+  if (!(sm_scale > 0.f) || !isfinite(sm_scale)) sm_scale = 1.0f / sqrtf((float)D);
+  DeviceGuard g(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  c->last_stream = st;
+  PrefillParams p;
+  p.q = static_cast<const __half*>(q);
+  p.ws_k = static_cast<const __half*>(ws_k);
+  p.ws_v = static_cast<const __half*>(ws_v);
+  p.cu_seqlens = cu_seqlens;
+  p.page_off = page_off;
+  p.out = static_cast<__half*>(out);
+  p.lse = lse;
+  p.n = n;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.num_ws_pages = ws_pages;
+  p.qscale = sm_scale * 1.4426950408889634f;
+  p.err = c->err;
+  return launch_prefill(p, D, max_len, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
 }
 
 ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {

@@ -47,7 +47,7 @@ EXPORTED = ["ekv_create", "ekv_destroy", "ekv_paged_decode", "ekv_gather_prefill
             "ekv_demote_pages", "ekv_get_error", "ekv_profile_enable", "ekv_profile_read",
             "ekv_set_decode_variant", "ekv_query", "ekv_paged_decode_noalloc",
             "ekv_demote_pages_base", "ekv_promote_pages", "ekv_append_kv", "ekv_paged_decode_elastic",
-            "ekv_transition_pages", "ekv_status_string"]
+            "ekv_transition_pages", "ekv_prefill_attention", "ekv_status_string"]
 
 
 class ekv_config(ctypes.Structure):
@@ -71,6 +71,7 @@ _lib.ekv_promote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
 _lib.ekv_paged_decode_elastic.argtypes = [_vp, _vp, _vp, _vp, _ll, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _i, _vp,
                                           _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp]
 _lib.ekv_transition_pages.argtypes = [_vp, _i, _vp, _ll, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp]
+_lib.ekv_prefill_attention.argtypes = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, ctypes.c_float, _vp, _vp, _vp]
 _lib.ekv_append_kv.argtypes = [_vp, _vp, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i, _vp, _i, _vp]
 _lib.ekv_paged_decode_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i,
                                           _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp]
@@ -210,6 +211,14 @@ def ekv_transition_pages(ctx, op, v_pages, v_page_stride_bytes, num_slots, num_p
     _check(_lib.ekv_transition_pages(ctx, op, _ptr(v_pages), v_page_stride_bytes, num_slots, num_pages,
                                      _ptr(page_ids), _ptr(src_loc), _ptr(dst_loc), n, _ptr(page_mode),
                                      _ptr(scale_out), _ptr(low), _stream(stream)), "ekv_transition_pages")
+
+
+def ekv_prefill_attention(ctx, q, ws_k, ws_v, ws_pages, cu_seqlens, page_off, n, max_len, sm_scale, out,
+                          lse=None, stream=None):
+    """FP16 causal prefill of whole prompts over the gathered workspace."""
+    _check(_lib.ekv_prefill_attention(ctx, _ptr(q), _ptr(ws_k), _ptr(ws_v), ws_pages, _ptr(cu_seqlens),
+                                      _ptr(page_off), n, max_len, float(sm_scale), _ptr(out), _ptr(lse),
+                                      _stream(stream)), "ekv_prefill_attention")
 
 
 def ekv_append_kv(ctx, k_new, v_new, k_pages, v_pages, v_page_stride_bytes, num_pages, v_scales,

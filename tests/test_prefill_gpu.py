@@ -1,0 +1,121 @@
+"""GPU parity of ekv_prefill_attention (FP16 causal prefill over the gathered workspace)
+against the float64 oracle: small ragged prompts compared on every row (a one-token
+prompt, page- and block-boundary lengths, GQA at two shapes), long prompts on sampled
+rows, the gather -> prefill chain on a mixed-fidelity cache, and a prompt longer than
+max_len reported."""
+
+import numpy as np
+import pytest
+
+from mixed_precision_paged_gb300 import workloads as wl
+from oracle import gather as og
+from oracle import prefill as op
+
+from _helpers import LSE_ATOL, OUT_ATOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+def _case(lens, H_q, H_kv, D, seed, slack=2):
+    rng = np.random.default_rng(seed)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    npages = [(l + 15) // 16 for l in lens]
+    page_off = (np.concatenate([[0], np.cumsum(npages)[:-1]]) + 1).astype(np.int32)   # page 0 unused
+    W = sum(npages) + slack + 1
+    q = rng.standard_normal((int(cu[-1]), H_q, D)).astype(np.float16)
+    ws_k = rng.standard_normal((W, 16, H_kv, D)).astype(np.float16)
+    ws_v = rng.standard_normal((W, 16, H_kv, D)).astype(np.float16)
+    return q, ws_k, ws_v, cu, page_off
+
+
+def _run(ekv_lib, torch, q, ws_k, ws_v, cu, po, H_q, H_kv, D, max_len=None):
+    T = q.shape[0]
+    ctx = ekv_lib.Context(H_q, H_kv, D, 1)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    out = torch.full((T, H_q, D), float("nan"), dtype=torch.float16, device="cuda")
+    lse = torch.full((T, H_q), float("nan"), dtype=torch.float32, device="cuda")
+    lens = np.diff(cu)
+    ekv_lib.ekv_prefill_attention(ctx.handle, t(q), t(ws_k), t(ws_v), ws_k.shape[0], t(cu), t(po), len(lens),
+                                  int(lens.max()) if max_len is None else max_len, 0.0, out, lse)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy(), ctx.error()
+
+
+def _check(out, lse, ref_out, ref_lse, rows):
+    e = np.abs(out[rows] - ref_out[rows]).max()
+    assert e <= OUT_ATOL, f"max-abs error {e:.3e}"
+    le = np.abs(lse[rows] - ref_lse[rows]).max()
+    assert le <= LSE_ATOL, f"lse error {le:.3e}"
+
+
+@pytest.mark.parametrize("H_q,H_kv,D", [(8, 2, 64), (32, 8, 128), (12, 4, 128), (4, 4, 64)])
+def test_small_prompts_every_row(ekv_lib, torch_cuda, H_q, H_kv, D):
+    lens = [1, 17, 64, 65, 130, 200]
+    q, k, v, cu, po = _case(lens, H_q, H_kv, D, 140 + D + H_q)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D)
+    assert err == (0, 0)
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
+    _check(out, lse, ref_out, ref_lse, np.arange(q.shape[0]))
+
+
+def test_long_prompts_sampled_rows(ekv_lib, torch_cuda):
+    lens = [2048, 1500, 3000]
+    H_q, H_kv, D = 32, 8, 128
+    q, k, v, cu, po = _case(lens, H_q, H_kv, D, 150)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D)
+    assert err == (0, 0)
+    sample = {0: [0, 63, 64, 1000, 2047], 1: [5, 1499], 2: [127, 128, 2999]}
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po, rows=sample)
+    rows = np.array([cu[i] + s for i, ss in sample.items() for s in ss])
+    _check(out, lse, ref_out, ref_lse, rows)
+
+
+def test_gather_then_prefill(ekv_lib, torch_cuda):
+    torch = torch_cuda
+    lens = [300, 97, 500]
+    H_q, H_kv, D = 32, 8, 128
+    case = wl.make_decode_case(lens, H_q, H_kv, D, v_format="mixed", scale_mode=1, seed=151, pool_pages=70,
+                               poison=False, p_compact=0.4, p_base=0.3)
+    pr = np.array([[b, 0, (l + 15) // 16] for b, l in enumerate(lens)])
+    total = int(pr[:, 2].sum())
+    t = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    ws_k = torch.empty((total, 16, H_kv, D), dtype=torch.float16, device="cuda")
+    ws_v = torch.empty_like(ws_k)
+    idx = torch.empty((total,), dtype=torch.int32, device="cuda")
+    ctx = ekv_lib.Context(H_q, H_kv, D, len(lens))
+    ekv_lib.ekv_gather_prefill(ctx.handle, t(case.k_pages), t(case.v_pages), case.v_page_stride, case.num_pages,
+                               t(case.v_scales), 1, t(case.page_mode), 0, t(case.block_table),
+                               case.block_table.shape[1], len(lens), pr, ws_k, ws_v, idx, total)
+    rng = np.random.default_rng(152)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    po = np.concatenate([[0], np.cumsum(pr[:, 2])[:-1]]).astype(np.int32)
+    q = rng.standard_normal((int(cu[-1]), H_q, D)).astype(np.float16)
+    out = torch.empty((q.shape[0], H_q, D), dtype=torch.float16, device="cuda")
+    lse = torch.empty((q.shape[0], H_q), dtype=torch.float32, device="cuda")
+    ekv_lib.ekv_prefill_attention(ctx.handle, t(q), ws_k, ws_v, total, t(cu), t(po), len(lens), int(max(lens)),
+                                  0.0, out, lse)
+    torch.cuda.synchronize()
+    assert ctx.error() == (0, 0)
+    rk, rv, _ = og.gather_prefill(case.k_pages, case.v_pages, case.v_scales, 1, case.page_mode, 0,
+                                  case.block_table, pr)
+    assert np.array_equal(ws_v.cpu().numpy().view(np.uint16), rv.view(np.uint16))
+    sample = {0: [0, 150, 299], 1: [96], 2: [0, 255, 256, 499]}
+    ref_out, ref_lse = op.prefill_attention(q, rk, rv, cu, po, rows=sample)
+    rows = np.array([cu[i] + s for i, ss in sample.items() for s in ss])
+    _check(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, rows)
+
+
+def test_prompt_longer_than_max_len_is_reported(ekv_lib, torch_cuda):
+    q, k, v, cu, po = _case([40, 200], 8, 2, 64, 153)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, 8, 2, 64, max_len=64)
+    assert err == (ekv_lib.EKV_ERR_DEVICE_CHECK, ekv_lib.EKV_DETAIL_SEQ_LEN)
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po, prompts=[0])
+    _check(out, lse, ref_out, ref_lse, np.arange(40))   # the short prompt is whole
