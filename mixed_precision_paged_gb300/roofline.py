@@ -100,3 +100,13 @@ def append_bytes(batch, num_kv_heads, head_dim, v_bytes):
     row = num_kv_heads * head_dim
     return batch * (row * (2 + 2 + 2 + v_bytes) + 4 + 4 + (4 * num_kv_heads if v_bytes == 1 else 0))
 
+
+def prefill_flops(prompt_lens, num_q_heads, head_dim):
+    """Algorithmic FLOPs of ``ekv_prefill_attention``: per prompt, query head and query
+    position s, 2 * (s + 1) * D for QK^T and the same for PV (causal: keys 0 .. s)."""
+    total = 0
+    for L in prompt_lens:
+        L = int(L)
+        total += 4 * head_dim * num_q_heads * (L * (L + 1) // 2)
+    return total
+
