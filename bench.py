@@ -401,20 +401,25 @@ def companions(ekv, torch, peaks):
     outp = torch.empty_like(qp)
     cu_p = torch.arange(0, (n_pr + 1) * L_pr, L_pr, dtype=torch.int32, device="cuda")
     po_p = torch.arange(0, n_pr * 512, 512, dtype=torch.int32, device="cuda")
-    pctx = ekv.Context(H * 4, H, D, 1)
-    ekv.ekv_prefill_attention(pctx.handle, qp, ws_k, ws_v, 4096, cu_p, po_p, n_pr, L_pr, 0.0, outp)
-    torch.cuda.synchronize()
-    tps = []
-    for _ in range(3):
-        s.record()
+    t_pf, perr, outs = {}, {}, {}
+    for variant, name in ((0, "tcgen05"), (1, "mma_sync")):
+        pctx = ekv.Context(H * 4, H, D, 1, variant=variant)
         ekv.ekv_prefill_attention(pctx.handle, qp, ws_k, ws_v, 4096, cu_p, po_p, n_pr, L_pr, 0.0, outp)
-        e.record()
         torch.cuda.synchronize()
-        tps.append(s.elapsed_time(e))
-    t_pf = float(np.median(tps))
+        tps = []
+        for _ in range(3):
+            s.record()
+            ekv.ekv_prefill_attention(pctx.handle, qp, ws_k, ws_v, 4096, cu_p, po_p, n_pr, L_pr, 0.0, outp)
+            e.record()
+            torch.cuda.synchronize()
+            tps.append(s.elapsed_time(e))
+        t_pf[name] = float(np.median(tps))
+        perr[name] = list(pctx.error())
+        outs[name] = outp.clone()
+        pctx.close()
     pf_flop = rf.prefill_flops([L_pr] * n_pr, H * 4, D)
-    perr = pctx.error()
-    pctx.close()
+    pf_agree = float((outs["tcgen05"].float() - outs["mma_sync"].float()).abs().max())
+    del outs
     del qp, outp
     # cache writer: one new token for each of the 32 sequences per call (latency-bound)
     k_new = torch.randn((32, H, D), generator=g, device="cuda").to(torch.float16)
@@ -444,10 +449,12 @@ def companions(ekv, torch, peaks):
                            "bytes": bb, "what": "the same 8,192 pages -> BASE high bytes + low-byte backing"},
            "promote": {"ms": t_p, "GB/s": bb / t_p / 1e6, "frac_of_measured_hbm": bb / t_p / 1e6 / hbm,
                        "bytes": bb, "what": "BASE -> TARGET from the backing", "exact_round_trip": exact},
-           "prefill": {"ms": t_pf, "TFLOP/s": pf_flop / t_pf / 1e9, "flop": pf_flop,
-                       "frac_of_measured_bf16": pf_flop / t_pf / 1e9 / peaks["bf16_tflops"],
+           "prefill": {"ms": t_pf["tcgen05"], "TFLOP/s": pf_flop / t_pf["tcgen05"] / 1e9, "flop": pf_flop,
+                       "frac_of_measured_bf16": pf_flop / t_pf["tcgen05"] / 1e9 / peaks["bf16_tflops"],
                        "what": "causal FP16 prefill, 8 prompts x 8192 tokens, 32/8 heads, D 128, over the "
-                               "4,096-page workspace (mma.sync flash-attention form)", "device_error": list(perr)},
+                               "4,096-page workspace (tcgen05 MMA, TMEM accumulators, TMA)",
+                       "mma_sync": {"ms": t_pf["mma_sync"], "TFLOP/s": pf_flop / t_pf["mma_sync"] / 1e9},
+                       "max_abs_diff_between_kernels": pf_agree, "device_error": perr},
            "append": {"us": t_a * 1e3, "GB/s": rf.append_bytes(32, H, D, 1) / t_a / 1e6,
                       "bytes": rf.append_bytes(32, H, D, 1),
                       "what": "one token for each of 32 sequences into E4M3 pages (launch-latency bound)"},

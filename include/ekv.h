@@ -197,7 +197,8 @@ ekv_status ekv_gather_prefill(ekv_ctx* ctx, const void* k_pages, const void* v_p
  *  ws_k, ws_v   fp16 [ws_pages][16][H_kv][D] (the gather's workspace), 16-byte aligned.
  *  cu_seqlens   DEVICE int32 [n + 1], nondecreasing; page_off DEVICE int32 [n].
  *  max_len      HOST int >= every len_i (sizes the grid); a longer prompt is reported
- *               (EKV_DETAIL_SEQ_LEN) and its later rows are not written.
+ *               (EKV_DETAIL_SEQ_LEN): its first max_len rows are computed (causal rows
+ *               need no later key) and its later rows are not written.
  *  lse          fp32 [T][H_q] (natural log) or NULL.
  * A prompt whose pages fall outside [0, ws_pages) is reported (EKV_DETAIL_PAGE_ID). */
 ekv_status ekv_prefill_attention(ekv_ctx* ctx, const void* q, const void* ws_k, const void* ws_v,
@@ -336,9 +337,11 @@ ekv_status ekv_get_error(ekv_ctx* ctx, int* code, int* detail);
 ekv_status ekv_profile_enable(ekv_ctx* ctx, int enable);
 ekv_status ekv_profile_read(ekv_ctx* ctx, double* split_ms, long long* launches);
 
-/* Decode consumer variant of this context: 0 (default) multiplies the QK and PV
- * tiles on the tensor cores (mma.sync f16 -> f32); 1 uses CUDA-core FP32 FMAs. Both
- * share the page pipeline and compute the same function; 1 exists for measurement. */
+/* Consumer variant of this context. Decode: 0 (default) multiplies the QK and PV
+ * tiles on the tensor cores (mma.sync f16 -> f32); 1 uses CUDA-core FP32 FMAs. Prefill
+ * (ekv_prefill_attention): 0 runs on the fifth-generation tensor cores (tcgen05 MMA,
+ * tensor-memory accumulators, TMA loads), 1 on warp-level mma.sync. Both variants
+ * compute the same function; 1 exists for measurement. */
 ekv_status ekv_set_decode_variant(ekv_ctx* ctx, int variant);
 
 /* Number of SMs and split-K CTAs per decode launch the context uses. */

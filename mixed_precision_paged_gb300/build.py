@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libekv.so")
-SOURCES = ["ekv_api.cu", "decode_simt.cu", "decode_mma.cu", "gather_demote.cu", "noalloc.cu", "prefill_mma.cu"]
+SOURCES = ["ekv_api.cu", "decode_simt.cu", "decode_mma.cu", "gather_demote.cu", "noalloc.cu", "prefill_mma.cu", "prefill_tc05.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -11,25 +11,13 @@
 #include "decode.cuh"
 #include "gather_demote.cuh"
 #include "pool_maps.h"
+#include "prefill.cuh"
 
 namespace ekv {
 cudaError_t launch_split_simt(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
                               const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_split_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
                              const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st);
-struct PrefillParams {
-  const __half* q;
-  const __half* ws_k;
-  const __half* ws_v;
-  const int32_t* cu_seqlens;
-  const int32_t* page_off;
-  __half* out;
-  float* lse;
-  int n, Hq, Hkv, G, num_ws_pages;
-  float qscale;
-  int* err;
-};
-cudaError_t launch_prefill(const PrefillParams& p, int D, int max_len, cudaStream_t st);
 }  // namespace ekv
 
 using namespace ekv;
@@ -463,9 +451,11 @@ ekv_status ekv_prefill_attention(ekv_ctx* c, const void* q, const void* ws_k, co
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
   p.num_ws_pages = ws_pages;
+  p.max_len = max_len;
   p.qscale = sm_scale * 1.4426950408889634f;
   p.err = c->err;
-  return launch_prefill(p, D, max_len, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+  const cudaError_t e = c->variant == 1 ? launch_prefill(p, D, max_len, st) : launch_prefill_tc05(p, D, max_len, st);
+  return e == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
 }
 
 ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {

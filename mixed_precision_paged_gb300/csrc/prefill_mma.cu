@@ -16,21 +16,9 @@
 // into the A fragments of O += P V (V fragments by ldmatrix.trans); l accumulates the
 // rounded P. CTAs with more work (later query blocks) are launched first.
 #include "common.cuh"
+#include "prefill.cuh"
 
 namespace ekv {
-
-struct PrefillParams {
-  const __half* q;             // [T][Hq][D]
-  const __half* ws_k;          // [W][16][Hkv][D]
-  const __half* ws_v;
-  const int32_t* cu_seqlens;   // [n + 1]
-  const int32_t* page_off;     // [n]
-  __half* out;                 // [T][Hq][D]
-  float* lse;                  // [T][Hq] or null
-  int n, Hq, Hkv, G, num_ws_pages;
-  float qscale;                // sm_scale * log2(e)
-  int* err;
-};
 
 namespace {
 
@@ -86,10 +74,11 @@ prefill_kernel(const PrefillParams p) {
   extern __shared__ __align__(128) uint8_t sm[];
   const int i = blockIdx.z, hq = blockIdx.y;
   const int row0 = __ldg(p.cu_seqlens + i);
-  const int L = __ldg(p.cu_seqlens + i + 1) - row0;
+  const int len = __ldg(p.cu_seqlens + i + 1) - row0;
   const int q0 = ((int)gridDim.x - 1 - (int)blockIdx.x) * kBM;   // heavier blocks first
-  if (blockIdx.x == 0 && threadIdx.x == 0 && L > (int)gridDim.x * kBM)   // longer than max_len
+  if (blockIdx.x == 0 && threadIdx.x == 0 && len > p.max_len)     // reported, rows cut there
     report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_SEQ_LEN, i);
+  const int L = min(len, p.max_len);
   if (q0 >= L) return;
   const int h = hq / p.G;
   const int pg0 = __ldg(p.page_off + i);

@@ -1,8 +1,10 @@
 """GPU parity of ekv_prefill_attention (FP16 causal prefill over the gathered workspace)
-against the float64 oracle: small ragged prompts compared on every row (a one-token
-prompt, page- and block-boundary lengths, GQA at two shapes), long prompts on sampled
-rows, the gather -> prefill chain on a mixed-fidelity cache, and a prompt longer than
-max_len reported."""
+against the float64 oracle, for both kernels (variant 0: tcgen05 tensor cores with
+tensor-memory accumulators; variant 1: warp-level mma.sync): small ragged prompts compared
+on every row (a one-token prompt, page-, key-block- and query-tile-boundary lengths, GQA
+at several shapes), scores that grow along the prompt (forcing the running max to be
+re-based), long prompts on sampled rows, the gather -> prefill chain on a mixed-fidelity
+cache, and a prompt longer than max_len reported and cut there."""
 
 import numpy as np
 import pytest
@@ -14,6 +16,7 @@ from oracle import prefill as op
 from _helpers import LSE_ATOL, OUT_ATOL
 
 pytestmark = pytest.mark.gpu
+VARIANTS = [0, 1]
 
 
 @pytest.fixture(scope="module")
@@ -36,9 +39,9 @@ def _case(lens, H_q, H_kv, D, seed, slack=2):
     return q, ws_k, ws_v, cu, page_off
 
 
-def _run(ekv_lib, torch, q, ws_k, ws_v, cu, po, H_q, H_kv, D, max_len=None):
+def _run(ekv_lib, torch, q, ws_k, ws_v, cu, po, H_q, H_kv, D, max_len=None, variant=0):
     T = q.shape[0]
-    ctx = ekv_lib.Context(H_q, H_kv, D, 1)
+    ctx = ekv_lib.Context(H_q, H_kv, D, 1, variant=variant)
     t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     out = torch.full((T, H_q, D), float("nan"), dtype=torch.float16, device="cuda")
     lse = torch.full((T, H_q), float("nan"), dtype=torch.float32, device="cuda")
@@ -56,21 +59,54 @@ def _check(out, lse, ref_out, ref_lse, rows):
     assert le <= LSE_ATOL, f"lse error {le:.3e}"
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("H_q,H_kv,D", [(8, 2, 64), (32, 8, 128), (12, 4, 128), (4, 4, 64)])
-def test_small_prompts_every_row(ekv_lib, torch_cuda, H_q, H_kv, D):
+def test_small_prompts_every_row(ekv_lib, torch_cuda, H_q, H_kv, D, variant):
     lens = [1, 17, 64, 65, 130, 200]
     q, k, v, cu, po = _case(lens, H_q, H_kv, D, 140 + D + H_q)
-    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D, variant=variant)
     assert err == (0, 0)
     ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
     _check(out, lse, ref_out, ref_lse, np.arange(q.shape[0]))
 
 
-def test_long_prompts_sampled_rows(ekv_lib, torch_cuda):
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("D", [64, 128])
+def test_tile_boundaries_every_row(ekv_lib, torch_cuda, D, variant):
+    # 64-key blocks, 128-row query tiles and 256-row CTAs: lengths on and around each
+    lens = [63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 385, 513]
+    H_q, H_kv = 4, 2
+    q, k, v, cu, po = _case(lens, H_q, H_kv, D, 160 + D)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D, variant=variant)
+    assert err == (0, 0)
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
+    _check(out, lse, ref_out, ref_lse, np.arange(q.shape[0]))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("D", [64, 128])
+def test_growing_scores_rebase_the_max(ekv_lib, torch_cuda, D, variant):
+    # keys grow along the prompt, so each row's running max climbs by many powers of two
+    # across its key blocks (the lazy re-basing of O and l must run, repeatedly)
+    lens = [700, 300]
+    H_q, H_kv = 4, 1
+    q, k, v, cu, po = _case(lens, H_q, H_kv, D, 170 + D)
+    q = np.abs(q.astype(np.float32)).astype(np.float16)
+    ramp = (0.1 * np.arange(k.shape[0] * 16, dtype=np.float32) / 16).reshape(k.shape[0], 16, 1, 1)
+    k = (np.abs(k.astype(np.float32)) * ramp).astype(np.float16)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D, variant=variant)
+    assert err == (0, 0)
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
+    assert np.all(np.isfinite(ref_lse))
+    _check(out, lse, ref_out, ref_lse, np.arange(q.shape[0]))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_long_prompts_sampled_rows(ekv_lib, torch_cuda, variant):
     lens = [2048, 1500, 3000]
     H_q, H_kv, D = 32, 8, 128
     q, k, v, cu, po = _case(lens, H_q, H_kv, D, 150)
-    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D, variant=variant)
     assert err == (0, 0)
     sample = {0: [0, 63, 64, 1000, 2047], 1: [5, 1499], 2: [127, 128, 2999]}
     ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po, rows=sample)
@@ -78,7 +114,8 @@ def test_long_prompts_sampled_rows(ekv_lib, torch_cuda):
     _check(out, lse, ref_out, ref_lse, rows)
 
 
-def test_gather_then_prefill(ekv_lib, torch_cuda):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_gather_then_prefill(ekv_lib, torch_cuda, variant):
     torch = torch_cuda
     lens = [300, 97, 500]
     H_q, H_kv, D = 32, 8, 128
@@ -90,7 +127,7 @@ def test_gather_then_prefill(ekv_lib, torch_cuda):
     ws_k = torch.empty((total, 16, H_kv, D), dtype=torch.float16, device="cuda")
     ws_v = torch.empty_like(ws_k)
     idx = torch.empty((total,), dtype=torch.int32, device="cuda")
-    ctx = ekv_lib.Context(H_q, H_kv, D, len(lens))
+    ctx = ekv_lib.Context(H_q, H_kv, D, len(lens), variant=variant)
     ekv_lib.ekv_gather_prefill(ctx.handle, t(case.k_pages), t(case.v_pages), case.v_page_stride, case.num_pages,
                                t(case.v_scales), 1, t(case.page_mode), 0, t(case.block_table),
                                case.block_table.shape[1], len(lens), pr, ws_k, ws_v, idx, total)
@@ -113,9 +150,11 @@ def test_gather_then_prefill(ekv_lib, torch_cuda):
     _check(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, rows)
 
 
-def test_prompt_longer_than_max_len_is_reported(ekv_lib, torch_cuda):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prompt_longer_than_max_len_is_reported(ekv_lib, torch_cuda, variant):
     q, k, v, cu, po = _case([40, 200], 8, 2, 64, 153)
-    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, 8, 2, 64, max_len=64)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, 8, 2, 64, max_len=64, variant=variant)
     assert err == (ekv_lib.EKV_ERR_DEVICE_CHECK, ekv_lib.EKV_DETAIL_SEQ_LEN)
-    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po, prompts=[0])
-    _check(out, lse, ref_out, ref_lse, np.arange(40))   # the short prompt is whole
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
+    _check(out, lse, ref_out, ref_lse, np.arange(40 + 64))   # the short prompt whole, the long one's first 64
+    assert np.all(np.isnan(out[40 + 64:]))                    # its later rows untouched
