@@ -465,6 +465,44 @@ def companions(ekv, torch, peaks):
 
 # ----------------------------------------------------------------------------- main
 
+def run_prefill_only(args):
+    """The FP16 causal prefill alone (32/8 heads, D 128) on PROMPTS x TOKENS over a
+    workspace of exactly their pages; prints one JSON line (ms per call, TFLOP/s)."""
+    import torch
+    from mixed_precision_paged_gb300 import build
+    build.ensure_built()
+    from mixed_precision_paged_gb300 import ekv
+    from mixed_precision_paged_gb300 import roofline as rf
+    n, L = args.prefill_only
+    Hq, Hkv, D = 32, 8, 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(args.seed)
+    pages = (L + 15) // 16
+    ws_k = torch.randn((n * pages, 16, Hkv, D), generator=g, device="cuda").to(torch.float16)
+    ws_v = torch.randn((n * pages, 16, Hkv, D), generator=g, device="cuda").to(torch.float16)
+    q = torch.randn((n * L, Hq, D), generator=g, device="cuda").to(torch.float16)
+    out = torch.empty_like(q)
+    cu = torch.arange(0, (n + 1) * L, L, dtype=torch.int32, device="cuda")
+    po = torch.arange(0, n * pages, pages, dtype=torch.int32, device="cuda")
+    ctx = ekv.Context(Hq, Hkv, D, 1, variant=args.variant)
+    for _ in range(args.warmup):
+        ekv.ekv_prefill_attention(ctx.handle, q, ws_k, ws_v, n * pages, cu, po, n, L, 0.0, out)
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        ekv.ekv_prefill_attention(ctx.handle, q, ws_k, ws_v, n * pages, cu, po, n, L, 0.0, out)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    flop = rf.prefill_flops([L] * n, Hq, D)
+    peaks, src = load_peaks()
+    print(json.dumps({"prefill_only": f"{n} x {L}", "variant": args.variant, "ms": ms,
+                      "TFLOP/s": flop / ms / 1e9, "frac_of_bf16": flop / ms / 1e9 / peaks["bf16_tflops"],
+                      "peak_source": src, "device_error": list(ctx.error())}))
+    ctx.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -478,11 +516,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-companions", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--prefill-only", type=int, nargs=2, metavar=("PROMPTS", "TOKENS"),
+                    help="time only the FP16 causal prefill on PROMPTS x TOKENS (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.prefill_only:
+        return run_prefill_only(args)
 
     import torch
     import torch.distributed as dist

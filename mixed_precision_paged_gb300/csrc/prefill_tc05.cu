@@ -8,28 +8,35 @@
 // workspace pages page_off[i], page_off[i] + 1, ... ([W][16][Hkv][D]).
 //
 // One CTA computes 256 query rows (two tiles of 128, the MMA's M) of one query head
-// against the key/value blocks of 64 tokens of its KV head up to the diagonal:
-//   warp 0       TMA producer: K and V blocks into a ring of NS stages, in the order the
-//                MMA warp uses them (K0, K1, V0, K2, V1, K3, ...); zeroes the value rows
-//                past the prompt in the last block, so that P = 0 never meets a NaN;
-//   warp 1       MMA issuer (one thread): S_t,j = Q_t K_j^T (SS form, both K-major) into
-//                tensor memory, O_t += P_t,j V_j (TS form: P from tensor memory, V
-//                N-major in shared memory);
+// against the key/value blocks of 128 tokens of its KV head up to the diagonal:
+//   warp 0       TMA producer: K and V blocks into a ring of NS stages in the order the
+//                MMA warp uses them (K0, V0, K1, V1, ...); zeroes the value rows past the
+//                prompt in the last block, so that P = 0 never meets a NaN;
+//   warp 1       MMA issuer (one thread): S_t = Q_t K_j^T (SS form, both K-major) and
+//                O_t += P_t V_j (TS form: P from tensor memory, V N-major in shared
+//                memory), tiles interleaved so that one tile's softmax overlaps the other
+//                tile's MMAs;
 //   warp 2       allocates and frees the 512 tensor-memory columns;
 //   warps 4..7   softmax of query tile 0, warps 8..11 of tile 1 (thread = query row):
-//                load the tile's Q rows into shared memory, then per key block read S,
-//                mask the diagonal, update the running max, write P = exp2(S' - m) as
-//                fp16 over the first half of S's own columns, and at the end normalise
-//                O and write out and lse.
-// Tensor memory, tile t: S/P buffers (64 columns each, alternating by key block) at
-// 256t and 256t + 64, O (D fp32 columns) at 256t + 128. The S of block j + 2 overwrites
-// P of block j only after the MMA warp has seen O += P_j V_j complete. Every mbarrier is
-// waited phase by phase (a parity wait is only defined within one phase of the barrier):
-// the softmax warps see each O += P V of their tile before handing over the next P.
+//                load the tile's Q rows into shared memory, then per key block read S
+//                (a max pass and an exponential pass over 32-column chunks), mask the
+//                diagonal block, update the running max, write P = exp2(S' - m) as fp16
+//                over the first half of S's columns, and at the end normalise O and write
+//                out and lse.
+// Tensor memory, tile t: S/P at 256t (128 columns), O at 256t + 128 (D fp32 columns).
+// The MMA warp issues S of block j + 1 over P of block j only after O += P_j V_j has
+// completed; the softmax of block j + 1 therefore never waits for the tensor core, and
+// may rescale O at any time before it hands over P.
+// The instruction stream of the MMA warp is the scarce resource: one tcgen05.mma or
+// tcgen05.commit issues every ~45 cycles per SM whatever its size, so the MMAs are the
+// largest the tensor memory allows (N = 128 for S, N = D for O) and their descriptors are
+// one 32-bit add from a precomputed base.
 // The running max is re-based lazily: O and l are rescaled only when a row's max grows by
 // more than 2^8 (the exponentials stay <= 256, exact to fp16's relative precision), so
 // most blocks touch O not at all. l sums the fp32 exponentials.
-// Every wait is bounded (1 s): a timeout is reported and every role winds down.
+// Every mbarrier is waited phase by phase (a parity wait is only defined within one phase
+// of the barrier); every wait is bounded (1 s): a timeout is reported and every role
+// winds down.
 #include "common.cuh"
 #include "pool_maps.h"
 #include "prefill.cuh"
@@ -40,7 +47,7 @@ namespace ekv {
 namespace {
 
 constexpr int kQRows = 128;                 // rows of a query tile (MMA M)
-constexpr int kKB = 64;                     // keys per K / V block
+constexpr int kKB = 128;                    // keys per K / V block (S's N)
 constexpr int kTThreads = 384;
 constexpr float kRebase = 8.f;              // log2 growth of the max that forces a rescale
 
@@ -49,7 +56,7 @@ struct TcCfg {
   static constexpr int NB = D / 64;                  // 128-byte slabs of a row
   static constexpr int QB = kQRows * D * 2;          // bytes of a query tile
   static constexpr int IB = kKB * D * 2;             // bytes of a K or V block
-  static constexpr int NS = D == 128 ? 10 : 16;      // ring stages
+  static constexpr int NS = D == 128 ? 5 : 12;       // ring stages
 };
 
 template <int NS>
@@ -59,8 +66,8 @@ struct TcBars {
   uint64_t mma_final;            // every MMA issued has completed
   uint64_t kv_full[NS];          // TMA bytes landed
   uint64_t kv_empty[NS];         // the MMAs reading the stage have completed
-  uint64_t s_full[2][2];         // [tile][buffer]: S written
-  uint64_t p_full[2][2];         // [tile][buffer]: P written, S read (128 arrivals)
+  uint64_t s_full[2];            // [tile]: S of the next block written
+  uint64_t p_full[2];            // [tile]: P written, S read (128 arrivals)
   uint64_t pv_done[2];           // [tile]: O += P V of the block completed
   uint32_t tmem_base;
   int abort;
@@ -92,9 +99,45 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
+// max of three (one instruction on sm_100+)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), one packed FP32 instruction
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// (a0, a1) += (b0, b1), one packed FP32 instruction
+__device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb;\n\t"
+      "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+      "add.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Warp-wide store of 16 columns (thread t: lane base + t).
+__device__ __forceinline__ void tst16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
 }
 
 }  // namespace
@@ -123,16 +166,16 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     if (threadIdx.x == 0 && qb == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, i);
     return;
   }
-  // key blocks of 64 each tile needs: up to its last row's diagonal, and not past the prompt
+  // key blocks each tile needs: up to its own (diagonal) block, and not past the prompt
   const int nkb = (L + kKB - 1) / kKB;
-  const int nt0 = min(q0 / kKB + 2, nkb);
-  const int nt1 = q0 + kQRows < L ? min(q0 / kKB + 4, nkb) : 0;
+  const int nt0 = min(q0 / kKB + 1, nkb);
+  const int nt1 = q0 + kQRows < L ? min(q0 / kKB + 2, nkb) : 0;
   const int n = max(nt0, nt1);
   const int zr = L - (n - 1) * kKB;          // value rows >= zr of the last block are zeroed
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;                                     // [2][NB][128 rows][128 B]
-  uint8_t* sKV = base + 2 * C::QB;                        // [NS][NB][64 rows][128 B]
+  uint8_t* sKV = base + 2 * C::QB;                        // [NS][NB][128 rows][128 B]
   TcBars<NS>* bars = reinterpret_cast<TcBars<NS>*>(sKV + NS * C::IB);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -146,10 +189,8 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
       mbar_init(&bars->kv_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(&bars->s_full[t][b], 1);
-        mbar_init(&bars->p_full[t][b], kQRows);
-      }
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], kQRows);
       mbar_init(&bars->pv_done[t], 1);
     }
     bars->abort = 0;
@@ -164,39 +205,39 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     const int tok0 = pg0 * kPage;
-    int u = 0;
-    auto issue = [&](int is_v, int j) -> bool {
-      const int s = u % NS;
-      if (u >= NS) {
-        bool ok = wait_bar(&bars->kv_empty[s], ((u / NS) - 1) & 1, abort);
-        if (!__all_sync(0xffffffffu, ok)) return false;
-      }
-      uint8_t* dst = sKV + s * C::IB;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->kv_full[s], C::IB);
-        tma_load_4d(dst, is_v ? &tv : &tk, 0, tok0 + j * kKB, 0, h, &bars->kv_full[s]);
-      }
-      if (is_v && j == n - 1 && zr < kKB) {
-        bool ok = wait_bar(&bars->kv_full[s], (u / NS) & 1, abort);
-        if (!__all_sync(0xffffffffu, ok)) return false;
-        const int per_slab = (kKB - zr) * 8;               // 16-byte chunks past the prompt
-        for (int e = lane; e < per_slab * C::NB; e += 32) {
-          const int slab = e / per_slab, rem = e % per_slab;
-          *reinterpret_cast<uint4*>(dst + slab * kKB * 128 + (zr + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->v_fixed);
-      }
-      ++u;
-      return true;
-    };
-    bool ok = issue(0, 0);
-    if (ok && n > 1) ok = issue(0, 1);
+    int stage = 0, u = 0;
+    uint32_t phase = 0;
+    bool ok = true;
     for (int j = 0; ok && j < n; ++j) {
-      ok = issue(1, j);
-      if (ok && j + 2 < n) ok = issue(0, j + 2);
+      for (int is_v = 0; is_v < 2; ++is_v) {
+        if (u >= NS) {                                      // the stage's previous item consumed
+          ok = __all_sync(0xffffffffu, wait_bar(&bars->kv_empty[stage], phase ^ 1u, abort));
+          if (!ok) break;
+        }
+        uint8_t* dst = sKV + stage * C::IB;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->kv_full[stage], C::IB);
+          tma_load_4d(dst, is_v ? &tv : &tk, 0, tok0 + j * kKB, 0, h, &bars->kv_full[stage]);
+        }
+        if (is_v && j == n - 1 && zr < kKB) {
+          ok = __all_sync(0xffffffffu, wait_bar(&bars->kv_full[stage], phase, abort));
+          if (!ok) break;
+          const int per_slab = (kKB - zr) * 8;             // 16-byte chunks past the prompt
+          for (int e = lane; e < per_slab * C::NB; e += 32) {
+            const int slab = e / per_slab, rem = e % per_slab;
+            *reinterpret_cast<uint4*>(dst + slab * kKB * 128 + (zr + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->v_fixed);
+        }
+        ++u;
+        if (++stage == NS) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
     }
     if (!ok && lane == 0) give_up(p.err, abort);
     // the copies still in flight land before the CTA can exit
@@ -210,69 +251,70 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     if (lane == 0) {
       constexpr uint32_t idS = tc05::idesc_f16_f32(kQRows, kKB, false);
       constexpr uint32_t idO = tc05::idesc_f16_f32(kQRows, D, true);
+      constexpr uint32_t HI = tc05::sdesc_hi(1024);        // 8-row groups 1024 B apart
       const int nt[2] = {nt0, nt1};
-      const uint32_t q_addr = smem_u32(sQ), kv_addr = smem_u32(sKV);
-      int u = 0;
-      bool ok = wait_bar(&bars->q_full, 0, abort);
-      // wait for item u; returns its shared address (0 on a failed wait)
-      auto take = [&](bool fixed) -> uint32_t {
-        const int s = u % NS;
-        const bool got = fixed ? wait_bar(&bars->v_fixed, 0, abort) : wait_bar(&bars->kv_full[s], (u / NS) & 1, abort);
-        if (!got) return 0u;
-        tc05::fence_after_sync();
-        return kv_addr + s * C::IB;
+      // descriptor low words: Q tile 0, K-major and V (N-major) views of ring stage 0
+      const uint32_t q_lo = tc05::sdesc_lo(smem_u32(sQ), 16);
+      const uint32_t k_lo = tc05::sdesc_lo(smem_u32(sKV), 16);
+      const uint32_t v_lo = tc05::sdesc_lo(smem_u32(sKV), kKB * 128);
+      // ring cursors of the K items (2j) and the V items (2j + 1)
+      int ks = 0, vs = 1;
+      uint32_t kp = 0, vp = 0;
+      auto adv2 = [&](int& s, uint32_t& ph) {
+        s += 2;
+        if (s >= NS) {
+          s -= NS;
+          ph ^= 1u;
+        }
       };
-      auto release = [&]() { tc05::commit(&bars->kv_empty[u % NS]); ++u; };
-      auto issue_s = [&](int t, int j, uint32_t kaddr) {
-        const uint32_t d = tbase + t * 256 + (j & 1) * kKB;
-        const uint32_t qa = q_addr + t * C::QB;
+      auto issue_s = [&](int t) {                          // S_t = Q_t K^T from stage ks
+        const uint32_t qa = q_lo + t * (C::QB >> 4), ka = k_lo + ks * (C::IB >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc05::mma_ss(d, tc05::sdesc_sw128(qa + (k >> 2) * (kQRows * 128) + (k & 3) * 32, 16, 1024),
-                       tc05::sdesc_sw128(kaddr + (k >> 2) * (kKB * 128) + (k & 3) * 32, 16, 1024), idS, k > 0);
-        tc05::commit(&bars->s_full[t][j & 1]);
+          tc05::mma_ss(tbase + t * 256, tc05::sdesc_join(qa + (((k >> 2) * (kQRows * 128) + (k & 3) * 32) >> 4), HI),
+                       tc05::sdesc_join(ka + (((k >> 2) * (kKB * 128) + (k & 3) * 32) >> 4), HI), idS, k > 0);
+        tc05::commit(&bars->s_full[t]);
       };
-      // prologue: S of key blocks 0 and 1 for both tiles
-      for (int j = 0; ok && j < 2 && j < n; ++j) {
-        const uint32_t ka = take(false);
-        ok = ka != 0u;
-        if (!ok) break;
+      bool ok = wait_bar(&bars->q_full, 0, abort) && wait_bar(&bars->kv_full[ks], kp, abort);
+      if (ok) {
+        tc05::fence_after_sync();
         for (int t = 0; t < 2; ++t)
-          if (j < nt[t]) issue_s(t, j, ka);
-        release();
+          if (nt[t] > 0) issue_s(t);
+        tc05::commit(&bars->kv_empty[ks]);
+        adv2(ks, kp);
       }
       for (int j = 0; ok && j < n; ++j) {
-        const uint32_t va = take(j == n - 1 && zr < kKB);
-        ok = va != 0u;
+        ok = (j == n - 1 && zr < kKB) ? wait_bar(&bars->v_fixed, 0, abort) : wait_bar(&bars->kv_full[vs], vp, abort);
         if (!ok) break;
+        tc05::fence_after_sync();
+        const uint32_t va = v_lo + vs * (C::IB >> 4);
+        bool k_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= nt[t]) continue;
-          ok = wait_bar(&bars->p_full[t][j & 1], (j >> 1) & 1, abort);
+          // O_t += P_t V_j once the softmax has written P
+          ok = wait_bar(&bars->p_full[t], j & 1, abort);
           if (!ok) break;
           tc05::fence_after_sync();
-          const uint32_t pa = tbase + t * 256 + (j & 1) * kKB;
+          const uint32_t pa = tbase + t * 256, od = tbase + t * 256 + 128;
 #pragma unroll
           for (int k = 0; k < kKB / 16; ++k)
-            tc05::mma_ts(tbase + t * 256 + 128, pa + 8 * k,
-                         tc05::sdesc_sw128(va + k * 2048, kKB * 128, 1024), idO, j > 0 || k > 0);
+            tc05::mma_ts(od, pa + 8 * k, tc05::sdesc_join(va + k * (2048 >> 4), HI), idO, j > 0 || k > 0);
           tc05::commit(&bars->pv_done[t]);
+          if (j + 1 < nt[t]) {
+            // S_t of block j + 1 overwrites P_t: after O_t += P_t V_j has completed
+            ok = (k_ready || wait_bar(&bars->kv_full[ks], kp, abort)) && wait_bar(&bars->pv_done[t], j & 1, abort);
+            if (!ok) break;
+            k_ready = true;
+            tc05::fence_after_sync();
+            issue_s(t);
+          }
         }
         if (!ok) break;
-        release();
-        if (j + 2 < n) {
-          const uint32_t ka = take(false);
-          ok = ka != 0u;
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j + 2 >= nt[t]) continue;
-            // P of block j (the buffer S of block j + 2 lands in) has been consumed
-            ok = wait_bar(&bars->pv_done[t], j & 1, abort);
-            if (ok) {
-              tc05::fence_after_sync();
-              issue_s(t, j + 2, ka);
-            }
-          }
-          if (!ok) break;
-          release();
+        tc05::commit(&bars->kv_empty[vs]);
+        adv2(vs, vp);
+        if (j + 1 < n) {
+          tc05::commit(&bars->kv_empty[ks]);
+          adv2(ks, kp);
         }
       }
       if (!ok) give_up(p.err, abort);
@@ -303,46 +345,37 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     const float qs = p.qscale;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    const uint32_t t_o = tbase + t * 256 + 128 + lanebase;
+    const uint32_t t_s = tbase + t * 256 + lanebase, t_o = tbase + t * 256 + 128 + lanebase;
     for (int j = 0; j < nmine; ++j) {
-      const uint32_t t_s = tbase + t * 256 + (j & 1) * kKB + lanebase;
-      ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full[t][j & 1], (j >> 1) & 1, abort));
+      ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full[t], j & 1, abort));
       if (!ok) break;
       tc05::fence_after_sync();
-      float x[kKB];
-      {
-        uint32_t a[32], b[32];
-        tc05::ld32(t_s, a);
-        tc05::ld32(t_s + 32, b);
-        tc05::wait_ld();
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] = __uint_as_float(a[c]);
-          x[32 + c] = __uint_as_float(b[c]);
-        }
-      }
       const int k0 = j * kKB;
-      if (k0 + kKB - 1 > q0 + t * kQRows) {               // the block reaches past some row
+      const bool diag = k0 + kKB - 1 > q0 + t * kQRows;   // the block reaches past some row
+      // pass 1: the row max over the block, 32 columns at a time
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < kKB / 32; ++c) {
+        uint32_t a[32];
+        tc05::ld32(t_s + 32 * c, a);
+        tc05::wait_ld();
+        float x[32];
 #pragma unroll
-        for (int c = 0; c < kKB; ++c)
-          if (k0 + c > prow) x[c] = -INFINITY;
+        for (int e = 0; e < 32; ++e) x[e] = (diag && k0 + 32 * c + e > prow) ? -INFINITY : __uint_as_float(a[e]);
+        float mg[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float* y = x + 8 * g;
+          mg[g] = fmaxf(max3f(max3f(y[0], y[1], y[2]), y[3], y[4]), max3f(y[5], y[6], y[7]));
+        }
+        mx = max3f(mx, max3f(mg[0], mg[1], mg[2]), mg[3]);
       }
-      float mx = x[0];
-#pragma unroll
-      for (int c = 1; c < kKB; ++c) mx = fmaxf(mx, x[c]);
       const float m_new = fmaxf(m_ref, mx * qs);
       const bool need = m_new > m_ref + kRebase;
-      // O += P V of block j - 1 is awaited once per block j >= 1 (here, or before P is
-      // handed over): a parity wait is only defined while the barrier is at most one
-      // phase away, so no pv_done phase may be skipped
-      bool pv_seen = j == 0;
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2f(m_ref - m_new) : 1.f;
-        if (j > 0) {                                       // O holds blocks < j: rescale it
-          ok = __all_sync(0xffffffffu, wait_bar(&bars->pv_done[t], (j - 1) & 1, abort));
-          if (!ok) break;
-          pv_seen = true;
-          tc05::fence_after_sync();
+        // O holds blocks < j, all complete (S of this block was issued after them)
+        if (j > 0) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -356,25 +389,39 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         l *= alpha;
         if (need) m_ref = m_new;
       }
+      // pass 2: P = exp2(S * scale - m) as fp16 over the first half of S's columns (chunk c
+      // writes columns 16c.., whose S values chunks <= c have already read)
       const float nm = -m_ref;
-      uint32_t pk[32];
+      float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int c = 0; c < kKB / 32; ++c) {
+        uint32_t a[32];
+        tc05::ld32(t_s + 32 * c, a);
+        tc05::wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2f(fmaf(x[2 * c], qs, nm)), p1 = ex2f(fmaf(x[2 * c + 1], qs, nm));
-        l += p0 + p1;
-        pk[c] = pack_half2(p0, p1);
+        for (int e = 0; e < 16; ++e) {
+          const int col = k0 + 32 * c + 2 * e;
+          float a0, a1;
+          ffma2(a0, a1, __uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]), qs, qs, nm, nm);
+          if (diag && col > prow) a0 = -INFINITY;
+          if (diag && col + 1 > prow) a1 = -INFINITY;
+          const float p0 = ex2f(a0), p1 = ex2f(a1);
+          fadd2(la[e & 3], lb[e & 3], p0, p1);
+          pk[e] = pack_half2(p0, p1);
+        }
+        tst16(t_s + 16 * c, pk);
       }
-      tc05::st32(t_s, pk);
+      fadd2(la[0], lb[0], la[2], lb[2]);
+      fadd2(la[1], lb[1], la[3], lb[3]);
+      l += (la[0] + la[1]) + (lb[0] + lb[1]);
       tc05::wait_st();
-      if (!pv_seen) {
-        ok = __all_sync(0xffffffffu, wait_bar(&bars->pv_done[t], (j - 1) & 1, abort));
-        if (!ok) break;
-      }
       tc05::fence_before_sync();
-      mbar_arrive(&bars->p_full[t][j & 1]);
+      mbar_arrive(&bars->p_full[t]);
     }
     if (!ok && lane == 0) give_up(p.err, abort);
     if (ok && nmine > 0) {
+      // the last O += P V of the tile (its commit covers every earlier one)
       ok = __all_sync(0xffffffffu, wait_bar(&bars->pv_done[t], (nmine - 1) & 1, abort));
       if (!ok && lane == 0) give_up(p.err, abort);
     }
@@ -411,7 +458,7 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 }
 
 // 4-D view (d mod 64, token, d / 64, KV head) of the workspace [W][16][Hkv][D] fp16; the
-// box {64, 64, D/64, 1} lands one key/value block as [D/64][64 rows][128 B], 128B swizzle.
+// box {64, 128, D/64, 1} lands one key/value block as [D/64][128 rows][128 B], 128B swizzle.
 static bool encode_ws_map(CUtensorMap* tm, const void* base, int D, int Hkv, int num_pages) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;

@@ -56,6 +56,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor as two 32-bit words: the start address lives in the low word only
+// (shared addresses stay below 2^18, so adding a byte offset / 16 never carries out of
+// its 14-bit field), so the descriptors of successive k-steps or ring stages are one
+// 32-bit add away from a base.
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
 // Instruction descriptor of a dense kind::f16 MMA with fp16 A and B, fp32 D, shape
 // M x N; `b_mn_major` selects an N-contiguous B (otherwise both are K-major).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
