@@ -33,7 +33,9 @@
 // one 32-bit add from a precomputed base.
 // The running max is re-based lazily: O and l are rescaled only when a row's max grows by
 // more than 2^8 (the exponentials stay <= 256, exact to fp16's relative precision), so
-// most blocks touch O not at all. l sums the fp32 exponentials.
+// most blocks touch O not at all. l sums the fp32 exponentials. The softmax is bound by
+// its instruction count, so the causal mask is a separate instance of each pass, run only
+// on the diagonal block.
 // Every mbarrier is waited phase by phase (a parity wait is only defined within one phase
 // of the barrier); every wait is bounded (1 s): a timeout is reported and every role
 // winds down.
@@ -138,6 +140,71 @@ __device__ __forceinline__ void tst16(uint32_t taddr, const uint32_t (&r)[16]) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+
+// Row max of one 128-column S block (tensor memory at t_s), 64 columns per load wait;
+// with MASK, columns whose key k0 + col follows the query prow count as -inf.
+template <bool MASK>
+__device__ __forceinline__ float block_max(uint32_t t_s, int k0, int prow) {
+  float mx = -INFINITY;
+#pragma unroll 1
+  for (int c = 0; c < kKB / 32; c += 2) {
+    uint32_t a[2][32];
+    tc05::ld32(t_s + 32 * c, a[0]);
+    tc05::ld32(t_s + 32 * c + 32, a[1]);
+    tc05::wait_ld();
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      float x[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        x[e] = (MASK && k0 + 32 * (c + h2) + e > prow) ? -INFINITY : __uint_as_float(a[h2][e]);
+      float mg[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const float* y = x + 8 * g;
+        mg[g] = fmaxf(max3f(max3f(y[0], y[1], y[2]), y[3], y[4]), max3f(y[5], y[6], y[7]));
+      }
+      mx = max3f(mx, max3f(mg[0], mg[1], mg[2]), mg[3]);
+    }
+  }
+  return mx;
+}
+
+// P = exp2(S * qs + nm) of one S block as fp16 over the first half of its columns (chunk
+// c writes columns 16c.., whose S values chunks <= c have already read); returns the sum
+// of the fp32 exponentials. MASK as for block_max.
+template <bool MASK>
+__device__ __forceinline__ float block_exp(uint32_t t_s, int k0, int prow, float qs, float nm) {
+  float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int c = 0; c < kKB / 32; c += 2) {
+    uint32_t a[2][32];
+    tc05::ld32(t_s + 32 * c, a[0]);
+    tc05::ld32(t_s + 32 * c + 32, a[1]);
+    tc05::wait_ld();
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float a0, a1;
+        ffma2(a0, a1, __uint_as_float(a[h2][2 * e]), __uint_as_float(a[h2][2 * e + 1]), qs, qs, nm, nm);
+        if (MASK) {
+          const int col = k0 + 32 * (c + h2) + 2 * e;
+          if (col > prow) a0 = -INFINITY;
+          if (col + 1 > prow) a1 = -INFINITY;
+        }
+        const float p0 = ex2f(a0), p1 = ex2f(a1);
+        fadd2(la[e & 3], lb[e & 3], p0, p1);
+        pk[e] = pack_half2(p0, p1);
+      }
+      tst16(t_s + 16 * (c + h2), pk);
+    }
+  }
+  fadd2(la[0], lb[0], la[2], lb[2]);
+  fadd2(la[1], lb[1], la[3], lb[3]);
+  return (la[0] + la[1]) + (lb[0] + lb[1]);
 }
 
 }  // namespace
@@ -352,24 +419,7 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
       tc05::fence_after_sync();
       const int k0 = j * kKB;
       const bool diag = k0 + kKB - 1 > q0 + t * kQRows;   // the block reaches past some row
-      // pass 1: the row max over the block, 32 columns at a time
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < kKB / 32; ++c) {
-        uint32_t a[32];
-        tc05::ld32(t_s + 32 * c, a);
-        tc05::wait_ld();
-        float x[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = (diag && k0 + 32 * c + e > prow) ? -INFINITY : __uint_as_float(a[e]);
-        float mg[4];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const float* y = x + 8 * g;
-          mg[g] = fmaxf(max3f(max3f(y[0], y[1], y[2]), y[3], y[4]), max3f(y[5], y[6], y[7]));
-        }
-        mx = max3f(mx, max3f(mg[0], mg[1], mg[2]), mg[3]);
-      }
+      const float mx = diag ? block_max<true>(t_s, k0, prow) : block_max<false>(t_s, k0, prow);
       const float m_new = fmaxf(m_ref, mx * qs);
       const bool need = m_new > m_ref + kRebase;
       if (__any_sync(0xffffffffu, need)) {
@@ -389,32 +439,7 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         l *= alpha;
         if (need) m_ref = m_new;
       }
-      // pass 2: P = exp2(S * scale - m) as fp16 over the first half of S's columns (chunk c
-      // writes columns 16c.., whose S values chunks <= c have already read)
-      const float nm = -m_ref;
-      float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int c = 0; c < kKB / 32; ++c) {
-        uint32_t a[32];
-        tc05::ld32(t_s + 32 * c, a);
-        tc05::wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = k0 + 32 * c + 2 * e;
-          float a0, a1;
-          ffma2(a0, a1, __uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]), qs, qs, nm, nm);
-          if (diag && col > prow) a0 = -INFINITY;
-          if (diag && col + 1 > prow) a1 = -INFINITY;
-          const float p0 = ex2f(a0), p1 = ex2f(a1);
-          fadd2(la[e & 3], lb[e & 3], p0, p1);
-          pk[e] = pack_half2(p0, p1);
-        }
-        tst16(t_s + 16 * c, pk);
-      }
-      fadd2(la[0], lb[0], la[2], lb[2]);
-      fadd2(la[1], lb[1], la[3], lb[3]);
-      l += (la[0] + la[1]) + (lb[0] + lb[1]);
+      l += diag ? block_exp<true>(t_s, k0, prow, qs, -m_ref) : block_exp<false>(t_s, k0, prow, qs, -m_ref);
       tc05::wait_st();
       tc05::fence_before_sync();
       mbar_arrive(&bars->p_full[t]);
