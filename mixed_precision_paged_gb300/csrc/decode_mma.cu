@@ -101,8 +101,9 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
   constexpr int KS = D / 16;   // k-steps of QK
   constexpr int MT = D / 16;   // m-tiles of PV
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hkv = p.Hkv, NG = p.NG, G = p.G;
-  const int h = warp % Hkv, grp = warp / Hkv;
+  const int Hkv = p.Hkv, G = p.G;
+  const int h = warp % Hkv;
+  const int v = (int)blockIdx.x * p.NG + warp / Hkv;    // this warp's range
   const int q4 = lane & 3, r8 = lane >> 2;          // fragment coordinates
   const bool uniform_scale = VMODE == kVE4M3 && p.scale_mode == EKV_SCALE_PER_TENSOR;
   // ldmatrix row address pattern (token, 16-byte chunk offset) of this lane
@@ -111,15 +112,15 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
   const int* cu = reinterpret_cast<const int*>(smem + p.cu_off);
   const WarpRing ring = warp_ring(p, smem, S::kBytes);
   const int n_range = end - start;
-  const int n_my = n_range > grp ? (n_range - grp + NG - 1) / NG : 0;   // this warp's pages
+  const int n_my = n_range;                          // this warp's pages
 
   // metadata of the warp's pages, 32 per batch, one per lane: cur = batch of k,
   // nxt = next batch (mode bytes / scales in flight), nxt2 = the one after (ids in flight)
   const float tensor_scale =
       (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR && p.v_scales) ? __ldg(p.v_scales) : 0.f;
   WarpMeta cur, nxt, nxt2;
-  wm_ids<EL>(p, cu, start, n_my, grp, lane, cur);
-  wm_ids<EL>(p, cu, start, n_my, grp, 32 + lane, nxt);
+  wm_ids<EL>(p, cu, start, n_my, lane, cur);
+  wm_ids<EL>(p, cu, start, n_my, 32 + lane, nxt);
   wm_meta<VMODE, EL>(p, tensor_scale, h, cur);
   {
     const int n0 = min(ring.nsl, n_my);              // prime the ring
@@ -130,7 +131,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
                            EL == kElYes, tmK, tmV8, tmV16);
   }
   wm_meta<VMODE, EL>(p, tensor_scale, h, nxt);
-  wm_ids<EL>(p, cu, start, n_my, grp, 64 + lane, nxt2);
+  wm_ids<EL>(p, cu, start, n_my, 64 + lane, nxt2);
   int k = 0;                                        // next page of this warp
   bool timed_out = false;
 
@@ -155,12 +156,12 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
     float l0 = 0.f, l1 = 0.f;                       // this lane's share of the sums
     bool seg_bad = false;                           // a page of this segment was skipped
     const int r_end = j1 - start;
-    for (; k < n_my && grp + k * NG < r_end; ++k) {
+    for (; k < r_end; ++k) {
       if ((k & 31) == 0 && k > 0) {                 // next metadata batch
         cur = nxt;
         nxt = nxt2;
         wm_meta<VMODE, EL>(p, tensor_scale, h, nxt);
-        wm_ids<EL>(p, cu, start, n_my, grp, k + 64 + lane, nxt2);
+        wm_ids<EL>(p, cu, start, n_my, k + 64 + lane, nxt2);
       }
       const int s_idx = k % ring.nsl;
       if (!mbar_wait(&ring.full[s_idx], (uint32_t)(k / ring.nsl) & 1u)) {
@@ -324,7 +325,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
     }
     if (timed_out) break;
     // ---- segment end (natural d order): the finished output when this warp saw the
-    // whole sequence (NG = 1 and no other CTA touches it), else a partial record
+    // whole sequence (no other range touches it), else a partial record
     float lt0 = l0, lt1 = l1;
 #pragma unroll
     for (int o = 4; o <= 16; o <<= 1) {
@@ -334,7 +335,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
     const float us = uniform_scale ? __ldg(p.v_scales) : 1.f;
     const int g0 = 2 * q4, g1 = 2 * q4 + 1;
     if (seg_bad) lt0 = lt1 = kBadRecord;
-    if (NG == 1 && !crosses_ctas(cu, b, start, end)) {
+    if (!crosses_ctas(cu, b, start, end)) {
       const float i0 = lt0 > 0.f ? us / lt0 : 0.f, i1 = lt1 > 0.f ? us / lt1 : 0.f;
       __half* ob = p.out + ((size_t)b * p.Hq + h * G) * D;
 #pragma unroll
@@ -352,7 +353,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
       }
       continue;
     }
-    const size_t R = (size_t)(b + blockIdx.x) * NG + grp;
+    const size_t R = (size_t)b + v;
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
       const int d = 16 * i + 2 * r8;
@@ -368,7 +369,7 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
       if (g1 < G) p.part_ml[R * p.Hq + h * G + g1] = make_float2(m1, lt1);
     }
   }
-  finish_warp<D>(p, cu, start, end, per, b_first, b_last, h, grp, merge_buf(ring, S::kBytes));
+  finish_warp<D>(p, cu, start, end, per, b_first, b_last, h, merge_buf(ring, S::kBytes));
 }
 
 template <int D, int VMODE, int EL>

@@ -26,26 +26,27 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
   constexpr int VPL = D / 32;
   constexpr int KB = D / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hkv = p.Hkv, NG = p.NG, G = p.G;
-  const int h = warp % Hkv, grp = warp / Hkv;
+  const int Hkv = p.Hkv, G = p.G;
+  const int h = warp % Hkv;
+  const int v = (int)blockIdx.x * p.NG + warp / Hkv;    // this warp's range
   const int tg = lane >> 3, c8 = lane & 7;
   float* pbuf = reinterpret_cast<float*>(smem + p.pbuf_off) + warp * (kPage * GP);
   const int* cu = reinterpret_cast<const int*>(smem + p.cu_off);
   const WarpRing ring = warp_ring(p, smem, S::kBytes);
   const int n_range = end - start;
-  const int n_my = n_range > grp ? (n_range - grp + NG - 1) / NG : 0;
+  const int n_my = n_range;
   const float tensor_scale =
       (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR && p.v_scales) ? __ldg(p.v_scales) : 0.f;
   WarpMeta cur, nxt, nxt2;
-  wm_ids<kElRuntime>(p, cu, start, n_my, grp, lane, cur);
-  wm_ids<kElRuntime>(p, cu, start, n_my, grp, 32 + lane, nxt);
+  wm_ids<kElRuntime>(p, cu, start, n_my, lane, cur);
+  wm_ids<kElRuntime>(p, cu, start, n_my, 32 + lane, nxt);
   wm_meta<VMODE, kElRuntime>(p, tensor_scale, h, cur);
   for (int kk = 0; kk < min(ring.nsl, n_my); ++kk)
     ring_issue<D, VMODE>(ring, kk, h, __shfl_sync(0xffffffffu, cur.page, kk),
                          __shfl_sync(0xffffffffu, cur.vloc, kk), __shfl_sync(0xffffffffu, cur.flags, kk),
                          p.elastic != 0, tmK, tmV8, tmV16);
   wm_meta<VMODE, kElRuntime>(p, tensor_scale, h, nxt);
-  wm_ids<kElRuntime>(p, cu, start, n_my, grp, 64 + lane, nxt2);
+  wm_ids<kElRuntime>(p, cu, start, n_my, 64 + lane, nxt2);
   int k = 0;
   bool timed_out = false;
 
@@ -80,12 +81,12 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
     }
     bool seg_bad = false;                          // a page of this segment was skipped
     const int r_end = j1 - start;
-    for (; k < n_my && grp + k * NG < r_end; ++k) {
+    for (; k < r_end; ++k) {
       if ((k & 31) == 0 && k > 0) {
         cur = nxt;
         nxt = nxt2;
         wm_meta<VMODE, kElRuntime>(p, tensor_scale, h, nxt);
-        wm_ids<kElRuntime>(p, cu, start, n_my, grp, k + 64 + lane, nxt2);
+        wm_ids<kElRuntime>(p, cu, start, n_my, k + 64 + lane, nxt2);
       }
       const int s_idx = k % ring.nsl;
       if (!mbar_wait(&ring.full[s_idx], (uint32_t)(k / ring.nsl) & 1u)) {
@@ -219,10 +220,10 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
       }
     }
     if (timed_out) break;
-    // the finished output when this warp saw the whole sequence (NG = 1 and no other
-    // CTA touches it), else the partial record of (segment b, this CTA, page group grp)
-    const bool direct = NG == 1 && !crosses_ctas(cu, b, start, end);
-    const size_t R = (size_t)(b + blockIdx.x) * NG + grp;
+    // the finished output when this warp saw the whole sequence (no other range touches
+    // it), else the partial record of (segment b, range v)
+    const bool direct = !crosses_ctas(cu, b, start, end);
+    const size_t R = (size_t)b + v;
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
       if (g >= G) break;
@@ -249,7 +250,7 @@ __device__ void consume_simt(const DecodeParams& p, const CUtensorMap* tmK, cons
       if (lane == 0) p.part_ml[R * p.Hq + h * G + g] = make_float2(m[g], ls);
     }
   }
-  finish_warp<D>(p, cu, start, end, per, b_first, b_last, h, grp, merge_buf(ring, S::kBytes));
+  finish_warp<D>(p, cu, start, end, per, b_first, b_last, h, merge_buf(ring, S::kBytes));
 }
 
 // --------------------------------------------------------------------- the kernel

@@ -3,18 +3,20 @@
 // per-warp metadata prefetch and the fused split merge.
 //
 // Work split: the pages of all sequences form one stream (cu = page prefix sum,
-// computed by every CTA from seq_lens); CTA c takes pages [c*per, (c+1)*per) of it,
-// per = ceil(total / gridDim.x), so every CTA streams the same number of pages
-// whatever the length mix. A CTA's range may cover several sequences (segments); it
-// writes one partial record per (segment, page group) at record (b + c) * NG + group,
-// which is unique because the CTAs that touch sequence b are exactly
-// cu[b]/per .. (cu[b+1]-1)/per and those ranges of consecutive sequences only meet
-// at one CTA. Records are written without any synchronisation as segments end; the
+// computed by every CTA from seq_lens), cut into gridDim.x * NG contiguous ranges of
+// per = ceil(total / (gridDim.x * NG)) pages, so every range holds the same number of
+// pages whatever the length mix. Warp w of CTA c owns KV head h = w % Hkv and page group
+// grp = w / Hkv (NG = 8 / Hkv groups) and streams range v = c * NG + grp: the warps of a
+// KV head work on contiguous ranges, so a sequence that lies inside one range is
+// finished by one warp with no merge at all. A range may cover several sequences
+// (segments); a segment of a sequence that other ranges also touch becomes a partial
+// record at index b + v, which is unique because the ranges that touch sequence b are
+// exactly cu[b]/per .. (cu[b+1]-1)/per and those of consecutive sequences only meet at
+// one range. Records are written without any synchronisation as segments end; the
 // merges happen when a warp's stream ends (finish_warp).
 //
-// Rings: warp w owns KV head h = w % Hkv and page group grp = w / Hkv (NG = 8 / Hkv
-// groups): it handles the slices (page r, head h) of the CTA's pages r = grp, grp + NG,
-// ... in order. Each warp keeps its own ring of `nsl` slots in shared memory and feeds
+// Rings: each warp handles the slices (page r, head h) of its range in order. Each warp
+// keeps its own ring of `nsl` slots in shared memory and feeds
 // it itself: lane 0 issues one TMA box for the K slice and one for the V slice,
 // 128B/64B-swizzled so that the warp's 16-byte row reads are bank-conflict free. A bulk
 // tensor copy stalls its issuing warp for about the same time whatever its size, so
@@ -112,7 +114,7 @@ struct WarpMeta {
 
 // Stage A: block-table entry of the warp's page k (consumed a batch later).
 template <int EL>
-__device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int start, int n_my, int grp, int k,
+__device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int start, int n_my, int k,
                                        WarpMeta& m) {
   m.page = 0;
   m.vloc = 0;
@@ -122,7 +124,7 @@ __device__ __forceinline__ void wm_ids(const DecodeParams& p, const int* cu, int
   m.b = -1;
   m.scale = 1.f;
   if (k < n_my) {
-    const int j = start + grp + k * p.NG;
+    const int j = start + k;
     const int b = upper_bound_i(cu, p.batch + 1, j) - 1;
     const int lp = j - cu[b];
     m.b = b;
@@ -250,16 +252,19 @@ __device__ __forceinline__ bool split_prologue(const DecodeParams& p, uint8_t* s
                                                int& end, int& per, int& b_first, int& b_last) {
   int* cu = reinterpret_cast<int*>(smem + p.cu_off);
   const int total = plan_pages(p, cu, warp_tot);
-  per = total > 0 ? (total + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+  const int nv = (int)gridDim.x * p.NG;                // ranges: one per (CTA, page group)
+  per = total > 0 ? (total + nv - 1) / nv : 1;
   if (blockIdx.x == 0) write_empty_sequences(p, cu);
-  start = (int)blockIdx.x * per;
-  end = min(total, start + per);
-  if (start >= end) return false;
+  if ((int)blockIdx.x * p.NG * per >= total) return false;   // the whole CTA is idle
   for (int i = threadIdx.x; i < kWarps * p.nsl; i += blockDim.x) {
     mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_barrier_init();
   }
   __syncthreads();
+  // this warp's range (no CTA-wide barrier follows, so an idle warp may leave here)
+  start = ((int)blockIdx.x * p.NG + (int)(threadIdx.x >> 5) / p.Hkv) * per;
+  end = min(total, start + per);
+  if (start >= end) return false;
   b_first = upper_bound_i(cu, p.batch + 1, start) - 1;
   b_last = upper_bound_i(cu, p.batch + 1, end - 1) - 1;
   return true;
@@ -274,8 +279,8 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* smem_raw) {
 // ------------------------------------------------------------------ fused merge
 // Partial results. A warp's result for (segment b, page group grp, KV head h) is
 //   m = max score (log2 units), l = sum 2^(s - m), acc = sum 2^(s - m) v
-// per query head. It is written as record (b + c) * NG + grp of CTA c, except when
-// the warp saw the whole sequence (NG = 1 and no other CTA touches it): then it writes
+// per query head. It is written as record b + v of range v, except when the warp saw
+// the whole sequence (no other range touches it): then it writes
 // the finished output directly. A warp that met a page it must skip (bad id, mode
 // byte or scale) writes l = -1 instead: the merge turns that into a zero output and
 // lse = -inf for the query heads of h.
@@ -411,25 +416,22 @@ __device__ void merge_run(const DecodeParams& p, int h, const MergeJob* jobs, in
   else merge_jobs<D, 8>(p, h, jobs, nj, mb.buf, mb.bytes);
 }
 
-// True when sequence b has pages outside this CTA's range [start, end).
+// True when sequence b has pages outside the range [start, end).
 __device__ __forceinline__ bool crosses_ctas(const int* cu, int b, int start, int end) {
   return cu[b] < start || cu[b + 1] > end;
 }
 
-// A warp's completion, after its stream ends (its records all written):
-//  * the sequences that continue in other CTAs (only the first and the last segment of
-//    the range can) take one ticket per warp for (b, h); the warp that takes the last
-//    of the n_cta * NG tickets merges (b, h) and resets the ticket;
-//  * with NG > 1, the sequences wholly inside the range are merged by the NG warps of
-//    head h after a barrier among those warps only, dealt round-robin.
-// Mid-stream segment ends take no fence and no atomic: the tickets of the CTA's first
-// segment are taken here too, which delays nothing, as its last records come from the
-// CTA before, finishing at about the same time.
+// A warp's completion, after its stream ends (its records all written): the sequences
+// that continue in other ranges (only the first and the last segment of a range can)
+// take one ticket per warp for (b, h); the warp that takes the last of the n ranges'
+// tickets merges (b, h) and resets the ticket. Mid-stream segment ends take no fence
+// and no atomic: the tickets of the range's first segment are taken here too, which
+// delays nothing, as its last records come from the range before, finishing at about
+// the same time.
 template <int D>
 __device__ void finish_warp(const DecodeParams& p, const int* cu, int start, int end, int per, int b_first,
-                            int b_last, int h, int grp, MergeBuf mb) {
+                            int b_last, int h, MergeBuf mb) {
   const int lane = threadIdx.x & 31;
-  const int NG = p.NG;
   int cross_b[2] = {-1, -1};
   int n_cross = 0;
   if (cu[b_first] != cu[b_first + 1] && crosses_ctas(cu, b_first, start, end)) cross_b[n_cross++] = b_first;
@@ -446,8 +448,8 @@ __device__ void finish_warp(const DecodeParams& p, const int* cu, int start, int
     }
     for (int e = 0; e < n_cross; ++e) {
       const int b = cross_b[e];
-      const int c0 = cu[b] / per, n_cta = (cu[b + 1] - 1) / per - c0 + 1;
-      if (old[e] == n_cta * NG - 1) {
+      const int n_ranges = (cu[b + 1] - 1) / per - cu[b] / per + 1;
+      if (old[e] == n_ranges - 1) {
         last_mask |= 1u << e;
         *tk[e] = 0;
       }
@@ -455,34 +457,13 @@ __device__ void finish_warp(const DecodeParams& p, const int* cu, int start, int
     if (last_mask) __threadfence();                    // other warps' records after their tickets
   }
   last_mask = __shfl_sync(0xffffffffu, last_mask, 0);
-  constexpr int kMaxJobs = 16;
-  MergeJob jobs[kMaxJobs];
+  MergeJob jobs[2];
   int nj = 0;
   for (int e = 0; e < n_cross; ++e) {
     if (!(last_mask & (1u << e))) continue;
     const int b = cross_b[e];
-    const int c0 = cu[b] / per, n_cta = (cu[b + 1] - 1) / per - c0 + 1;
-    jobs[nj++] = MergeJob{b, (b + c0) * NG, n_cta * NG};
-  }
-  // sequences wholly inside this CTA (NG > 1 only: with NG = 1 the consumer wrote them
-  // out directly): b_first + 1 .. b_last - 1, plus the ends when they do not cross
-  // (the same set for every warp of the CTA)
-  const int lo = (cu[b_first] == cu[b_first + 1] || crosses_ctas(cu, b_first, start, end)) ? b_first + 1 : b_first;
-  const int hi = crosses_ctas(cu, b_last, start, end) ? b_last - 1 : b_last;
-  if (NG > 1 && lo <= hi) {
-    // the NG warps of head h (warps h, h + Hkv, ...): their records of these sequences
-    // are complete after this barrier (ids 1..4; NG > 1 means Hkv <= 4)
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + h), "r"(32 * NG) : "memory");
-    int item = 0;
-    for (int b = lo; b <= hi; ++b) {
-      if (cu[b] == cu[b + 1]) continue;
-      if (item++ % NG != grp) continue;
-      if (nj == kMaxJobs) {
-        merge_run<D>(p, h, jobs, nj, mb);
-        nj = 0;
-      }
-      jobs[nj++] = MergeJob{b, (b + (int)blockIdx.x) * NG, NG};
-    }
+    const int v0 = cu[b] / per, n_ranges = (cu[b + 1] - 1) / per - v0 + 1;
+    jobs[nj++] = MergeJob{b, b + v0, n_ranges};
   }
   merge_run<D>(p, h, jobs, nj, mb);
 }
