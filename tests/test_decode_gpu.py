@@ -82,6 +82,21 @@ def test_long_sequences_split_across_many_ctas(ekv_lib, torch_cuda, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("lens,hq,hkv,d", [([4000], 8, 1, 128), ([3000, 5], 16, 2, 64)])
+def test_one_long_sequence_over_hundreds_of_ranges(ekv_lib, torch_cuda, variant, lens, hq, hkv, d):
+    # with few KV heads every warp streams its own page range (#SMs * 8 / H_kv ranges of
+    # about one page here), so one sequence is split into hundreds of records and its
+    # merge runs in many waves of staged records
+    case = wl.make_decode_case(lens, hq, hkv, d, v_format="mixed", scale_mode=1,
+                               pool_pages=sum((l + 15) // 16 for l in lens) + 3, seed=11 + hkv)
+    ctx = make_ctx(ekv_lib, case, variant)
+    out, lse = gpu_decode(ctx, to_device(case))
+    ref_out, ref_lse = oracle_decode(case)
+    assert_close(out, lse, ref_out, ref_lse)
+    assert ctx.error() == (0, 0)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 def test_many_short_sequences(ekv_lib, torch_cuda, variant):
     rng = np.random.default_rng(8)
     lens = list(rng.integers(0, 40, size=300))
