@@ -4,15 +4,15 @@
 //
 // Work split: the pages of all sequences form one stream (cu = page prefix sum,
 // computed by every CTA from seq_lens), cut into gridDim.x * NG contiguous ranges of
-// per = ceil(total / (gridDim.x * NG)) pages, so every range holds the same number of
-// pages whatever the length mix. Warp w of CTA c owns KV head h = w % Hkv and page group
+// equal cost, a page costing 1 and each sequence start kSegmentCost more (page j of
+// sequence b at position j + kSegmentCost * b; per = ceil(positions / ranges)), so every
+// range takes about the same time whatever the length mix. Warp w of CTA c owns KV head h = w % Hkv and page group
 // grp = w / Hkv (NG = 8 / Hkv groups) and streams range v = c * NG + grp: the warps of a
 // KV head work on contiguous ranges, so a sequence that lies inside one range is
 // finished by one warp with no merge at all. A range may cover several sequences
 // (segments); a segment of a sequence that other ranges also touch becomes a partial
 // record at index b + v, which is unique because the ranges that touch sequence b are
-// exactly cu[b]/per .. (cu[b+1]-1)/per and those of consecutive sequences only meet at
-// one range. Records are written without any synchronisation as segments end; the
+// consecutive (ranges_of) and those of consecutive sequences only meet at one range. Records are written without any synchronisation as segments end; the
 // merges happen when a warp's stream ends (finish_warp).
 //
 // Rings: each warp handles the slices (page r, head h) of its range in order. Each warp
@@ -35,6 +35,28 @@ __device__ __forceinline__ int upper_bound_i(const int* a, int n, int x) {
     if (a[mid] <= x) lo = mid + 1; else hi = mid;
   }
   return lo;
+}
+
+// Cost of starting a sequence in a page range, in pages: a segment's Q load, pipeline
+// restart and end record (swept 1..3 on a 256-sequence mix and on 32 x 8K: 2 is best).
+constexpr int kSegmentCost = 2;
+
+// The first page whose cost-stream position j + kSegmentCost * b is >= x (total if none):
+// b is the first sequence with cu[b + 1] + kSegmentCost * b > x.
+__device__ __forceinline__ int page_at(const int* cu, int batch, int x) {
+  int lo = 0, hi = batch;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid + 1] + kSegmentCost * mid <= x) lo = mid + 1; else hi = mid;
+  }
+  if (lo == batch) return cu[batch];
+  return max(cu[lo], x - kSegmentCost * lo);
+}
+
+// The ranges that hold pages of sequence b (non-empty): v0 .. v0 + n - 1.
+__device__ __forceinline__ void ranges_of(const int* cu, int b, int per, int& v0, int& n) {
+  v0 = (cu[b] + kSegmentCost * b) / per;
+  n = (cu[b + 1] - 1 + kSegmentCost * b) / per - v0 + 1;
 }
 
 // Sequences with no pages (length 0, or a length the block table cannot hold) are
@@ -252,18 +274,23 @@ __device__ __forceinline__ bool split_prologue(const DecodeParams& p, uint8_t* s
                                                int& end, int& per, int& b_first, int& b_last) {
   int* cu = reinterpret_cast<int*>(smem + p.cu_off);
   const int total = plan_pages(p, cu, warp_tot);
+  // ranges split the stream by cost: a page costs 1 and the start of a sequence (its Q
+  // load and segment end) kSegmentCost more, so page j of sequence b sits at position
+  // j + kSegmentCost * b of a stream of total + kSegmentCost * batch positions
   const int nv = (int)gridDim.x * p.NG;                // ranges: one per (CTA, page group)
-  per = total > 0 ? (total + nv - 1) / nv : 1;
+  const int vtotal = total + kSegmentCost * p.batch;
+  per = total > 0 ? (vtotal + nv - 1) / nv : 1;
   if (blockIdx.x == 0) write_empty_sequences(p, cu);
-  if ((int)blockIdx.x * p.NG * per >= total) return false;   // the whole CTA is idle
+  if (total == 0 || (int)blockIdx.x * p.NG * per >= vtotal) return false;   // the whole CTA is idle
   for (int i = threadIdx.x; i < kWarps * p.nsl; i += blockDim.x) {
     mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);
     fence_barrier_init();
   }
   __syncthreads();
   // this warp's range (no CTA-wide barrier follows, so an idle warp may leave here)
-  start = ((int)blockIdx.x * p.NG + (int)(threadIdx.x >> 5) / p.Hkv) * per;
-  end = min(total, start + per);
+  const int v = (int)blockIdx.x * p.NG + (int)(threadIdx.x >> 5) / p.Hkv;
+  start = page_at(cu, p.batch, v * per);
+  end = page_at(cu, p.batch, min(vtotal, (v + 1) * per));
   if (start >= end) return false;
   b_first = upper_bound_i(cu, p.batch + 1, start) - 1;
   b_last = upper_bound_i(cu, p.batch + 1, end - 1) - 1;
@@ -447,8 +474,8 @@ __device__ void finish_warp(const DecodeParams& p, const int* cu, int start, int
       old[e] = atomicAdd(tk[e], 1);
     }
     for (int e = 0; e < n_cross; ++e) {
-      const int b = cross_b[e];
-      const int n_ranges = (cu[b + 1] - 1) / per - cu[b] / per + 1;
+      int v0, n_ranges;
+      ranges_of(cu, cross_b[e], per, v0, n_ranges);
       if (old[e] == n_ranges - 1) {
         last_mask |= 1u << e;
         *tk[e] = 0;
@@ -462,7 +489,8 @@ __device__ void finish_warp(const DecodeParams& p, const int* cu, int start, int
   for (int e = 0; e < n_cross; ++e) {
     if (!(last_mask & (1u << e))) continue;
     const int b = cross_b[e];
-    const int v0 = cu[b] / per, n_ranges = (cu[b + 1] - 1) / per - v0 + 1;
+    int v0, n_ranges;
+    ranges_of(cu, b, per, v0, n_ranges);
     jobs[nj++] = MergeJob{b, b + v0, n_ranges};
   }
   merge_run<D>(p, h, jobs, nj, mb);
