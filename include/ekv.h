@@ -186,6 +186,27 @@ ekv_status ekv_gather_prefill(ekv_ctx* ctx, const void* k_pages, const void* v_p
                               void* ws_k, void* ws_v, int32_t* ws_indices, int ws_pages,
                               int apply_scale, void* stream);
 
+/* The compact-prefill gather from ElasticKV's pair-structured value layout (ElasticKV
+ * Sec. 3.1, Sec. 3.2): as ekv_gather_prefill, but the values of logical page j of
+ * sequence b are read at half-slot location v_block_table[b][j] (a TARGET page fills slot
+ * e/2, e even; a compact or BASE page is half e%2 of slot e/2), and a page's mode comes
+ * from boundaries (T-B-T: BASE for boundaries[b][0] <= j < boundaries[b][1]), else from
+ * page_mode / uniform_mode; has_base = 0 gathers every page as TARGET. Keys stay at the
+ * logical page. v_pages, num_v_slots, v_block_table, boundaries and has_base as for
+ * ekv_paged_decode_elastic (v_block_table must not be NULL). A location outside the pool,
+ * or an odd one for a TARGET page, is a device error (EKV_DETAIL_PAGE_ID) that zeroes the
+ * workspace page. */
+ekv_status ekv_gather_prefill_elastic(ekv_ctx* ctx, const void* k_pages, const void* v_pages,
+                                      long long v_page_stride_bytes, int num_pages, int num_v_slots,
+                                      const float* v_scales, int scale_mode,
+                                      const uint8_t* page_mode, int uniform_mode,
+                                      const int32_t* block_table, const int32_t* v_block_table,
+                                      int block_table_stride, const int32_t* boundaries,
+                                      int has_base, int block_table_rows,
+                                      const int32_t* page_range, int n, void* ws_k, void* ws_v,
+                                      int32_t* ws_indices, int ws_pages, int apply_scale,
+                                      void* stream);
+
 /* FP16 causal prefill of whole prompts over the gathered workspace (knlp.io "What
  * changes in vLLM's prefill routing?": after the gather casts the stored K16/V8 pages into
  * the bounded FP16 workspace, a native FP16 prefill runs over it; causal, no cached

@@ -242,12 +242,16 @@ ekv_status ekv_paged_decode_elastic(ekv_ctx* c, const void* q, const void* k_pag
                      seq_lens, batch, sm_scale, out, lse, stream);
 }
 
-ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pages,
-                              long long v_page_stride_bytes, int num_pages, const float* v_scales,
-                              int scale_mode, const uint8_t* page_mode, int uniform_mode,
-                              const int32_t* block_table, int block_table_stride, int block_table_rows,
-                              const int32_t* page_range, int n, void* ws_k, void* ws_v,
-                              int32_t* ws_indices, int ws_pages, int apply_scale, void* stream) {
+namespace {
+
+// The gather of both layouts: v_block_table null -> the plain layout (values at the
+// logical page id; num_v_slots, boundaries and has_base unused).
+ekv_status gather_impl(ekv_ctx* c, const void* k_pages, const void* v_pages, long long v_page_stride_bytes,
+                       int num_pages, int num_v_slots, const float* v_scales, int scale_mode,
+                       const uint8_t* page_mode, int uniform_mode, const int32_t* block_table,
+                       const int32_t* v_block_table, int block_table_stride, const int32_t* boundaries,
+                       int has_base, int block_table_rows, const int32_t* page_range, int n, void* ws_k,
+                       void* ws_v, int32_t* ws_indices, int ws_pages, int apply_scale, void* stream) {
   if (!c || n < 0 || ws_pages < 0) return EKV_ERR_INVALID_ARG;
   if (n == 0) return EKV_OK;
   const int Hkv = c->cfg.num_kv_heads, D = c->cfg.head_dim;
@@ -259,8 +263,10 @@ ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pag
   const bool any_compact = uniform_mode == EKV_MODE_COMPACT_E4M3;   // a mode table: checked per page
   const bool any_target = page_mode || uniform_mode != EKV_MODE_COMPACT_E4M3;
   const long long n_elem = (long long)kPage * Hkv * D;
-  if (v_page_stride_bytes < (any_target ? 2 * n_elem : n_elem) || (v_page_stride_bytes & 15))
+  // the pair-structured layout: every slot holds a TARGET page or two halves
+  if (v_page_stride_bytes < (v_block_table || any_target ? 2 * n_elem : n_elem) || (v_page_stride_bytes & 15))
     return EKV_ERR_INVALID_ARG;
+  if (v_block_table && num_v_slots < 1) return EKV_ERR_INVALID_ARG;
   if (any_compact && apply_scale && !v_scales) return EKV_ERR_INVALID_ARG;
   if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(ws_k) || !aligned16(ws_v))
     return EKV_ERR_INVALID_ARG;
@@ -295,6 +301,10 @@ ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pag
   p.D = D;
   p.apply_scale = apply_scale ? 1 : 0;
   p.err = c->err;
+  p.v_block_table = v_block_table;
+  p.num_v_slots = num_v_slots;
+  p.boundaries = v_block_table ? boundaries : nullptr;
+  p.has_base = v_block_table ? has_base : 1;
   int base = 0;
   for (int i0 = 0; i0 < n; i0 += kMaxRanges) {
     GatherRanges r;
@@ -313,6 +323,34 @@ ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pag
     base += off;
   }
   return EKV_OK;
+}
+
+}  // namespace
+
+ekv_status ekv_gather_prefill(ekv_ctx* c, const void* k_pages, const void* v_pages,
+                              long long v_page_stride_bytes, int num_pages, const float* v_scales,
+                              int scale_mode, const uint8_t* page_mode, int uniform_mode,
+                              const int32_t* block_table, int block_table_stride, int block_table_rows,
+                              const int32_t* page_range, int n, void* ws_k, void* ws_v,
+                              int32_t* ws_indices, int ws_pages, int apply_scale, void* stream) {
+  return gather_impl(c, k_pages, v_pages, v_page_stride_bytes, num_pages, 0, v_scales, scale_mode, page_mode,
+                     uniform_mode, block_table, nullptr, block_table_stride, nullptr, 1, block_table_rows,
+                     page_range, n, ws_k, ws_v, ws_indices, ws_pages, apply_scale, stream);
+}
+
+ekv_status ekv_gather_prefill_elastic(ekv_ctx* c, const void* k_pages, const void* v_pages,
+                                      long long v_page_stride_bytes, int num_pages, int num_v_slots,
+                                      const float* v_scales, int scale_mode, const uint8_t* page_mode,
+                                      int uniform_mode, const int32_t* block_table,
+                                      const int32_t* v_block_table, int block_table_stride,
+                                      const int32_t* boundaries, int has_base, int block_table_rows,
+                                      const int32_t* page_range, int n, void* ws_k, void* ws_v,
+                                      int32_t* ws_indices, int ws_pages, int apply_scale, void* stream) {
+  if (!v_block_table) return EKV_ERR_INVALID_ARG;
+  return gather_impl(c, k_pages, v_pages, v_page_stride_bytes, num_pages, num_v_slots, v_scales, scale_mode,
+                     page_mode, uniform_mode, block_table, v_block_table, block_table_stride, boundaries,
+                     has_base, block_table_rows, page_range, n, ws_k, ws_v, ws_indices, ws_pages, apply_scale,
+                     stream);
 }
 
 namespace {

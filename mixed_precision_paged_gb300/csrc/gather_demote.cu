@@ -30,10 +30,30 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
   if (tid == 0) p.ws_indices[w] = w;
   int mode = 0;
   int detail = (page < 0 || page >= p.num_pages) ? EKV_DETAIL_PAGE_ID : EKV_DETAIL_NONE;
+  int loc = 2 * page;                             // value location (half-slot index)
   if (detail == EKV_DETAIL_NONE) {
-    mode = p.page_mode ? (int)__ldg(p.page_mode + page) : p.uniform_mode;
-    if (mode > EKV_MODE_BASE) detail = EKV_DETAIL_PAGE_MODE;
-    else if (mode == EKV_MODE_COMPACT_E4M3 && p.apply_scale && !p.v_scales) detail = EKV_DETAIL_SCALE;
+    if (p.v_block_table) {                        // pair-structured layout
+      loc = __ldg(p.v_block_table + (size_t)r.seq[k] * p.bt_stride + lp);
+      if (!p.has_base) {
+        mode = EKV_MODE_TARGET_FP16;
+      } else if (p.boundaries) {                  // TARGET-BASE-TARGET: no mode lookup
+        const int b0 = __ldg(p.boundaries + 2 * r.seq[k]), b1 = __ldg(p.boundaries + 2 * r.seq[k] + 1);
+        mode = (lp >= b0 && lp < b1) ? EKV_MODE_BASE : EKV_MODE_TARGET_FP16;
+      } else {
+        mode = p.page_mode ? (int)__ldg(p.page_mode + page) : p.uniform_mode;
+      }
+      // a TARGET page fills a whole slot (even location); a compact or BASE page one half
+      if (loc < 0 || loc >= 2 * p.num_v_slots || (mode == EKV_MODE_TARGET_FP16 && (loc & 1)))
+        detail = EKV_DETAIL_PAGE_ID;
+    } else {
+      mode = p.page_mode ? (int)__ldg(p.page_mode + page) : p.uniform_mode;
+    }
+    if (detail != EKV_DETAIL_NONE) {
+    } else if (mode > EKV_MODE_BASE) {
+      detail = EKV_DETAIL_PAGE_MODE;
+    } else if (mode == EKV_MODE_COMPACT_E4M3 && p.apply_scale && !p.v_scales) {
+      detail = EKV_DETAIL_SCALE;
+    }
   }
   if (detail != EKV_DETAIL_NONE) {
     if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, detail, w);
@@ -59,7 +79,8 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
       if (v < nvec16) wk[v] = buf[u];
     }
   }
-  const uint8_t* vsrc = p.v_pages + (size_t)page * p.v_page_stride;
+  // a TARGET page at slot loc / 2; a compact or BASE page in half loc % 2 of that slot
+  const uint8_t* vsrc = p.v_pages + (size_t)(loc >> 1) * p.v_page_stride + (size_t)(loc & 1) * n_elem;
   if (mode == 0) {
     const uint4* sv = reinterpret_cast<const uint4*>(vsrc);
     uint4 buf[kVecPerThread];

@@ -32,6 +32,12 @@ struct GatherParams {
   int Hkv, D;
   int apply_scale;
   int* err;
+  // pair-structured value layout (ElasticKV): value location (half-slot index) of each
+  // logical page; null -> the plain layout (location 2 * page id)
+  const int32_t* v_block_table;
+  int num_v_slots;                // slots of v_pages (elastic layout only)
+  const int32_t* boundaries;      // [B][2] T-B-T boundaries or null (elastic layout only)
+  int has_base;                   // 0: every page TARGET (elastic layout only)
 };
 
 // Page-mode transitions run by the same streaming kernel.

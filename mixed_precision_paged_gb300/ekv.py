@@ -47,7 +47,8 @@ EXPORTED = ["ekv_create", "ekv_destroy", "ekv_paged_decode", "ekv_gather_prefill
             "ekv_demote_pages", "ekv_get_error", "ekv_profile_enable", "ekv_profile_read",
             "ekv_set_decode_variant", "ekv_query", "ekv_paged_decode_noalloc",
             "ekv_demote_pages_base", "ekv_promote_pages", "ekv_append_kv", "ekv_paged_decode_elastic",
-            "ekv_transition_pages", "ekv_prefill_attention", "ekv_status_string"]
+            "ekv_transition_pages", "ekv_prefill_attention", "ekv_gather_prefill_elastic",
+            "ekv_status_string"]
 
 
 class ekv_config(ctypes.Structure):
@@ -65,6 +66,8 @@ _lib.ekv_paged_decode.argtypes = [_vp, _vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i,
                                   _i, ctypes.c_float, _vp, _vp, _vp]
 _lib.ekv_gather_prefill.argtypes = [_vp, _vp, _vp, _ll, _i, _vp, _i, _vp, _i, _vp, _i, _i, _vp,
                                     _i, _vp, _vp, _vp, _i, _i, _vp]
+_lib.ekv_gather_prefill_elastic.argtypes = [_vp, _vp, _vp, _ll, _i, _i, _vp, _i, _vp, _i, _vp, _vp, _i, _vp,
+                                            _i, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _vp]
 _lib.ekv_demote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
 _lib.ekv_demote_pages_base.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
 _lib.ekv_promote_pages.argtypes = [_vp, _vp, _ll, _i, _vp, _i, _vp, _vp, _vp]
@@ -167,6 +170,20 @@ def ekv_gather_prefill(ctx, k_pages, v_pages, v_page_stride_bytes, num_pages, v_
                                    block_table_rows, pr.ctypes.data, pr.shape[0], _ptr(ws_k),
                                    _ptr(ws_v), _ptr(ws_indices), ws_pages, int(apply_scale),
                                    _stream(stream)), "ekv_gather_prefill")
+
+
+def ekv_gather_prefill_elastic(ctx, k_pages, v_pages, v_page_stride_bytes, num_pages, num_v_slots,
+                               v_scales, scale_mode, page_mode, uniform_mode, block_table, v_block_table,
+                               block_table_stride, boundaries, has_base, block_table_rows, page_range,
+                               ws_k, ws_v, ws_indices, ws_pages, apply_scale=1, stream=None):
+    pr = np.ascontiguousarray(np.asarray(page_range, dtype=np.int32).reshape(-1, 3))
+    _check(_lib.ekv_gather_prefill_elastic(ctx, _ptr(k_pages), _ptr(v_pages), v_page_stride_bytes,
+                                           num_pages, num_v_slots, _ptr(v_scales), scale_mode,
+                                           _ptr(page_mode), uniform_mode, _ptr(block_table),
+                                           _ptr(v_block_table), block_table_stride, _ptr(boundaries),
+                                           int(has_base), block_table_rows, pr.ctypes.data, pr.shape[0],
+                                           _ptr(ws_k), _ptr(ws_v), _ptr(ws_indices), ws_pages,
+                                           int(apply_scale), _stream(stream)), "ekv_gather_prefill_elastic")
 
 
 def ekv_demote_pages(ctx, v_pages, v_page_stride_bytes, num_pages, page_ids, n, page_mode,

@@ -17,6 +17,9 @@ Elastic KV Layout", Sec. 3.2 and App. B.3:
   TARGET page to a destination slot. Packing a pair (A, B) into A's slot is two
   transitions: A in place (half 0 of its slot), then B into half 1 of A's slot.
 
+* The compact-prefill gather reads each page's values at its location with the same
+  mode rules (``gather_prefill_elastic``).
+
 Pins: ``tests/test_oracle_elastic.py``.
 """
 
@@ -136,3 +139,41 @@ def transition(op, v_pages, page_ids, src, dst, page_mode, scale_out, low, H_kv,
                 lw[i] = (words & np.uint16(0xFF)).astype(np.uint8)
             m[p] = MODE_BASE
     return v, m, sc, lw
+
+
+def gather_prefill_elastic(k_pages, v_pages, v_scales, scale_mode, page_mode, uniform_mode, block_table,
+                           v_block_table, boundaries, has_base, page_range, apply_scale=True, S=PAGE_SIZE):
+    """Oracle of ``ekv_gather_prefill_elastic``: the plain gather definition
+    (``gather.gather_prefill``) applied to each page's values read at its location and its
+    mode taken from the boundaries, the mode table or the batch indicator. Built as a
+    plain pool of the gathered pages (page w = the w-th gathered page: its K page, its
+    value bytes, its mode and its scale row) and the plain gather over it."""
+    from . import gather
+    P, _, H_kv, D = k_pages.shape
+    n = S * H_kv * D
+    pages = []
+    for seq, first, num in np.asarray(page_range, dtype=np.int64).reshape(-1, 3):
+        for j in range(int(first), int(first) + int(num)):
+            pages.append((int(seq), j))
+    W = len(pages)
+    k_tmp = np.zeros((max(W, 1), S, H_kv, D), dtype=np.float16)
+    v_tmp = np.zeros((max(W, 1), 2 * n), dtype=np.uint8)
+    m_tmp = np.zeros(max(W, 1), dtype=np.uint8)
+    s_tmp = None if scale_mode != 1 or v_scales is None else np.ones((max(W, 1), H_kv), dtype=np.float32)
+    for w, (b, j) in enumerate(pages):
+        p = int(block_table[b][j])
+        loc = int(v_block_table[b][j])
+        mode = page_mode_of(b, j, p, page_mode, uniform_mode, boundaries, has_base)
+        k_tmp[w] = k_pages[p]
+        m_tmp[w] = mode
+        if mode == MODE_TARGET_FP16:
+            v_tmp[w] = slot_bytes(v_pages, loc, n)
+        else:
+            v_tmp[w][:n] = half_bytes(v_pages, loc, n)
+        if s_tmp is not None:
+            s_tmp[w] = np.asarray(v_scales, dtype=np.float32).reshape(-1, H_kv)[p]
+    scales = s_tmp if s_tmp is not None else v_scales
+    ws_k, ws_v, idx = gather.gather_prefill(k_tmp, v_tmp, scales, scale_mode, m_tmp, 0,
+                                            np.arange(max(W, 1), dtype=np.int32).reshape(1, -1),
+                                            np.array([[0, 0, W]]), apply_scale)
+    return ws_k, ws_v, idx

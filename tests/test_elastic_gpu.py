@@ -2,7 +2,8 @@
 the oracle: pairs packed into one value slot by two located transitions (BASE and E4M3),
 decode through the value block table (freed slots filled with garbage), the structured
 TARGET-BASE-TARGET boundaries, the batch-level has_base = 0 path, identity locations
-matching the plain decode bit for bit, and bad locations reported."""
+matching the plain decode bit for bit, bad locations reported, and the compact-prefill
+gather from the same layouts bit for bit."""
 
 import numpy as np
 import pytest
@@ -154,3 +155,79 @@ def test_bad_locations_are_reported(ekv_lib, torch_cuda):
     _transition(ekv_lib, torch, ctx, 1, case.v_pages, np.zeros(case.num_pages, np.uint8), [0], [0],
                 [2 * case.num_pages + 1], None, None, 2, 64)
     assert ctx.error() == (ekv_lib.EKV_ERR_DEVICE_CHECK, ekv_lib.EKV_DETAIL_PAGE_ID)
+
+
+def _gather(ekv_lib, torch, ctx, case, v_pages, page_mode, scales, scale_mode, vtab, bnd, has_base, pr):
+    total = int(np.asarray(pr)[:, 2].sum())
+    H, D = case.num_kv_heads, case.head_dim
+    ws_k = torch.full((total, 16, H, D), float("nan"), dtype=torch.float16, device="cuda")
+    ws_v = torch.full_like(ws_k, float("nan"))
+    idx = torch.empty((total,), dtype=torch.int32, device="cuda")
+    ekv_lib.ekv_gather_prefill_elastic(ctx.handle, _t(torch, case.k_pages), _t(torch, v_pages), v_pages.shape[1],
+                                       case.num_pages, v_pages.shape[0], _t(torch, scales), scale_mode,
+                                       _t(torch, page_mode), 0, _t(torch, case.block_table), _t(torch, vtab),
+                                       case.block_table.shape[1], _t(torch, bnd), has_base, case.batch, pr,
+                                       ws_k, ws_v, idx, total)
+    torch.cuda.synchronize()
+    return ws_k.cpu().numpy(), ws_v.cpu().numpy(), idx.cpu().numpy()
+
+
+@pytest.mark.parametrize("op", [oe.OP_TO_BASE, oe.OP_TO_E4M3])
+def test_gather_from_packed_pairs(ekv_lib, torch_cuda, op):
+    torch = torch_cuda
+    lens = [16 * 9, 16 * 7 + 5]
+    hkv, d = 4, 128
+    case = wl.make_decode_case(lens, 16, hkv, d, v_format="fp16", seed=140 + op, pool_pages=20, poison=False)
+    P, H = case.num_pages, hkv
+    ctx = ekv_lib.Context(16, hkv, d, len(lens))
+    bt = case.block_table
+    pairs = [(int(bt[b, j]), int(bt[b, j + 1])) for b in (0, 1) for j in (2, 4)]
+    a = [x for x, _ in pairs]
+    bb = [y for _, y in pairs]
+    mode = np.zeros(P, np.uint8)
+    scales = np.ones((P, H), np.float32)
+    v1, m1, s1, _ = _transition(ekv_lib, torch, ctx, op, case.v_pages, mode, a, None, None, scales, None, H, d)
+    v2, m2, s2, _ = _transition(ekv_lib, torch, ctx, op, v1, m1, bb, [2 * y for y in bb],
+                                [2 * x + 1 for x in a], s1, None, H, d)
+    vtab = 2 * bt.copy()
+    for x, y in pairs:
+        vtab[bt == y] = 2 * x + 1
+    for y in bb:                                      # freed slots: garbage
+        v2[y] = 0x7E
+    pr = np.array([[0, 0, 9], [1, 1, 7]])
+    gk, gv, gi = _gather(ekv_lib, torch, ctx, case, v2, m2, s2, 1, vtab, None, 1, pr)
+    assert ctx.error() == (0, 0)
+    rk, rv, ri = oe.gather_prefill_elastic(case.k_pages, v2, s2, 1, m2, 0, bt, vtab, None, 1, pr)
+    assert np.array_equal(gk.view(np.uint16), rk.view(np.uint16))
+    assert np.array_equal(gv.view(np.uint16), rv.view(np.uint16)) and np.array_equal(gi, ri)
+
+
+def test_gather_boundaries_has_base_and_bad_location(ekv_lib, torch_cuda):
+    torch = torch_cuda
+    lens = [16 * 8, 16 * 6 - 3]
+    hkv, d = 4, 64
+    case = wl.make_decode_case(lens, 8, hkv, d, v_format="fp16", seed=150, pool_pages=16, poison=False)
+    P = case.num_pages
+    bt = case.block_table
+    bnd = np.array([[2, 6], [1, 5]], np.int32)
+    base_pages = [int(bt[b, j]) for b in range(2) for j in range(bnd[b, 0], bnd[b, 1])]
+    ctx = ekv_lib.Context(8, hkv, d, 2)
+    v1, _, _, _ = _transition(ekv_lib, torch, ctx, oe.OP_TO_BASE, case.v_pages, np.zeros(P, np.uint8), base_pages,
+                              None, None, None, None, hkv, d)
+    pr = np.array([[0, 0, 8], [1, 0, 6]])
+    _, gv, _ = _gather(ekv_lib, torch, ctx, case, v1, None, None, 0, 2 * bt, bnd, 1, pr)
+    assert ctx.error() == (0, 0)
+    _, rv, _ = oe.gather_prefill_elastic(case.k_pages, v1, None, 0, None, 0, bt, 2 * bt, bnd, 1, pr)
+    assert np.array_equal(gv.view(np.uint16), rv.view(np.uint16))
+    # has_base = 0: the original TARGET pool, modes and boundaries ignored
+    _, gv, _ = _gather(ekv_lib, torch, ctx, case, case.v_pages, np.full(P, 2, np.uint8), None, 0, 2 * bt, bnd, 0, pr)
+    assert ctx.error() == (0, 0)
+    _, rv, _ = oe.gather_prefill_elastic(case.k_pages, case.v_pages, None, 0, np.full(P, 2, np.uint8), 0, bt,
+                                         2 * bt, bnd, 0, pr)
+    assert np.array_equal(gv.view(np.uint16), rv.view(np.uint16))
+    # an odd location for a TARGET page: reported, that workspace page zeroed
+    vtab = 2 * bt.copy()
+    vtab[1, 0] += 1
+    gk, gv, _ = _gather(ekv_lib, torch, ctx, case, case.v_pages, None, None, 0, vtab, None, 1, pr)
+    assert ctx.error() == (ekv_lib.EKV_ERR_DEVICE_CHECK, ekv_lib.EKV_DETAIL_PAGE_ID)
+    assert np.all(gv[8] == 0) and np.all(gk[8] == 0)

@@ -7,12 +7,14 @@ plain paths (decode, BASE and E4M3 demotion), not to its own formulas:
   place, and the freed slots are never read (garbage written there changes nothing);
 * TARGET-BASE-TARGET boundaries give the decode of the equivalent mode table;
 * has_base = 0 reads every page as TARGET, ignoring boundaries and the mode table;
-* promotion into a fresh slot restores the TARGET bytes exactly.
+* promotion into a fresh slot restores the TARGET bytes exactly;
+* the elastic gather equals the plain gather (identity locations; packed pairs against
+  the same pages demoted in place; boundaries against the mode table; has_base = 0).
 """
 
 import numpy as np
 
-from oracle import base, decode, demote, elastic
+from oracle import base, decode, demote, elastic, gather
 
 H, G, D, S = 2, 2, 64, 16
 N = S * H * D
@@ -107,3 +109,66 @@ def test_has_base_zero_reads_target_everywhere():
                                           np.array([[0, 7]], np.int32), 0, lens)
     ref, ref_l = decode.paged_decode(q, k, v, None, 0, None, 0, bt, lens)
     assert np.array_equal(out, ref) and np.array_equal(l, ref_l)
+
+
+def _gather_pair_case():
+    """Pairs of E4M3 and BASE pages packed into shared slots (two located transitions),
+    with the in-place demotion of the same pages as the reference pool."""
+    P = 12
+    k, x, v = _pool(P, 9)
+    bt = np.array([[0, 1, 2, 3, 4, 5], [6, 7, 8, 9, 10, 11]], np.int32)
+    modes = np.zeros(P, np.uint8)
+    sc = np.ones((P, H), np.float32)
+    # E4M3 pair (1, 2) and BASE pair (7, 8): A in place, then B into half 1 of A's slot
+    vp, modes, sc, _ = elastic.transition(elastic.OP_TO_E4M3, v, [1], None, None, modes, sc, None, H, D)
+    vp, modes, sc, _ = elastic.transition(elastic.OP_TO_E4M3, vp, [2], [4], [3], modes, sc, None, H, D)
+    vp, modes, sc, _ = elastic.transition(elastic.OP_TO_BASE, vp, [7], None, None, modes, sc, None, H, D)
+    vp, modes, sc, _ = elastic.transition(elastic.OP_TO_BASE, vp, [8], [16], [15], modes, sc, None, H, D)
+    vtab = 2 * bt.copy()
+    vtab[0, 2] = 3
+    vtab[1, 2] = 15
+    vp[2] = 0x7E                                        # freed slots: never read
+    vp[8] = 0x7E
+    rv, rm, rs = demote.demote_pages(v, [1, 2], np.zeros(P, np.uint8), np.ones((P, H), np.float32), H, D)
+    rb, rmb, _, _ = base.demote_to_base(rv, [7, 8], rm, H, D)
+    return k, vp, modes, sc, bt, vtab, rb, rmb, rs
+
+
+def test_elastic_gather_identity_locations_is_the_plain_gather():
+    k, x, v = _pool(10, 11)
+    modes = np.zeros(10, np.uint8)
+    v2, modes, sc, _ = elastic.transition(elastic.OP_TO_E4M3, v, [1, 5], None, None, modes,
+                                          np.ones((10, H), np.float32), None, H, D)
+    v2, modes, _, _ = elastic.transition(elastic.OP_TO_BASE, v2, [4, 7], None, None, modes, sc, None, H, D)
+    bt = np.array([[3, 1, 7, 0], [2, 4, 5, 6]], np.int32)
+    pr = np.array([[0, 0, 3], [1, 1, 3]])
+    ek, ev, ei = elastic.gather_prefill_elastic(k, v2, sc, 1, modes, 0, bt, 2 * bt, None, 1, pr)
+    rk, rv, ri = gather.gather_prefill(k, v2, sc, 1, modes, 0, bt, pr)
+    assert np.array_equal(ek.view(np.uint16), rk.view(np.uint16))
+    assert np.array_equal(ev.view(np.uint16), rv.view(np.uint16)) and np.array_equal(ei, ri)
+
+
+def test_elastic_gather_of_packed_pairs_is_the_gather_of_in_place_demotion():
+    k, vp, modes, sc, bt, vtab, rb, rmb, rs = _gather_pair_case()
+    pr = np.array([[0, 0, 6], [1, 0, 6]])
+    ek, ev, _ = elastic.gather_prefill_elastic(k, vp, sc, 1, modes, 0, bt, vtab, None, 1, pr)
+    rk, rv, _ = gather.gather_prefill(k, rb, rs, 1, rmb, 0, bt, pr)
+    assert np.array_equal(ek.view(np.uint16), rk.view(np.uint16))
+    assert np.array_equal(ev.view(np.uint16), rv.view(np.uint16))
+
+
+def test_elastic_gather_boundaries_and_has_base():
+    P = 14
+    k, x, v = _pool(P, 12)
+    bt = np.array([[0, 1, 2, 3, 4, 5, 0], [6, 7, 8, 9, 10, 11, 12]], np.int32)
+    bnd = np.array([[2, 5], [1, 7]], np.int32)
+    base_pages = [bt[0, j] for j in range(2, 5)] + [bt[1, j] for j in range(1, 7)]
+    vb, modes, _, _ = base.demote_to_base(v, base_pages, np.zeros(P, np.uint8), H, D)
+    pr = np.array([[0, 0, 6], [1, 0, 7]])
+    ek, ev, _ = elastic.gather_prefill_elastic(k, vb, None, 0, None, 0, bt, 2 * bt, bnd, 1, pr)
+    rk, rv, _ = gather.gather_prefill(k, vb, None, 0, modes, 0, bt, pr)
+    assert np.array_equal(ev.view(np.uint16), rv.view(np.uint16))
+    # has_base = 0: the original TARGET pool, modes and boundaries ignored
+    ek, ev, _ = elastic.gather_prefill_elastic(k, v, None, 0, np.full(P, 2, np.uint8), 2, bt, 2 * bt, bnd, 0, pr)
+    rk, rv, _ = gather.gather_prefill(k, v, None, 0, None, 0, bt, pr)
+    assert np.array_equal(ev.view(np.uint16), rv.view(np.uint16))
