@@ -13,9 +13,10 @@ e2e          the same metric through the C ABI with the per-step inputs (q, bloc
 roofline     split kernel's algorithmic bytes / its own event-timed duration, against
              the measured HBM copy peak
 cpu_baseline the float64 oracle on the host cores, on a sample of the same workload
-companions   gather + demotion on the 32 x 8192-token gather/demote workload
+companions   gather, demotion (E4M3, BASE), promotion, append and FP16 prefill on their
+             workloads (32 x 8192-token prompts; 8 x 8192 for prefill)
 
---impl reference times the float64 oracle (the reference arm of this build) on the
+--impl reference times the float64 oracle (there is no other reference program) on the
 host cores, on bounded samples of the same workload.
 """
 
