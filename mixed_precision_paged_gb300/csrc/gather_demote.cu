@@ -427,7 +427,17 @@ cudaError_t launch_transition(const DemoteParams& p, int op, int n, int num_sms,
 // whose scale is missing or not positive finite keeps its old bytes. All reported.
 __global__ void __launch_bounds__(128)
 append_kernel(const AppendParams p) {
+  // three dependent global round trips: the position, the page id, then the mode byte and
+  // the scale together; the new row (which depends on neither) is loaded first
   const int b = blockIdx.x, tid = threadIdx.x;
+  const int row_elems = p.Hkv * p.D;
+  const int v = tid;                              // vector of 8 values
+  const bool mine = 8 * v < row_elems;
+  uint4 kx = make_uint4(0u, 0u, 0u, 0u), vx = kx;
+  if (mine) {
+    kx = __ldg(reinterpret_cast<const uint4*>(p.k_new + (size_t)b * row_elems) + v);
+    vx = __ldg(reinterpret_cast<const uint4*>(p.v_new + (size_t)b * row_elems) + v);
+  }
   const int t = __ldg(p.positions + b);
   if (t < 0) return;
   if (t >= p.bt_stride * kPage) {
@@ -439,18 +449,18 @@ append_kernel(const AppendParams p) {
     if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, b);
     return;
   }
+  const int head = mine ? (8 * v) / p.D : 0;
   const int mode = p.page_mode ? (int)__ldg(p.page_mode + page) : p.uniform_mode;
+  const float s = !p.v_scales ? 0.f
+                  : (p.scale_mode == EKV_SCALE_PER_TENSOR ? __ldg(p.v_scales)
+                                                           : __ldg(p.v_scales + (size_t)page * p.Hkv + head));
   if (mode > EKV_MODE_BASE) {
     if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_MODE, b);
     return;
   }
-  const int row_elems = p.Hkv * p.D;
+  if (!mine) return;
   const int row = t % kPage;
-  const int v = tid;                              // vector of 8 values
-  if (8 * v >= row_elems) return;
-  const uint4 kx = __ldg(reinterpret_cast<const uint4*>(p.k_new + (size_t)b * row_elems) + v);
   reinterpret_cast<uint4*>(p.k_pages + ((size_t)page * kPage + row) * row_elems)[v] = kx;
-  const uint4 vx = __ldg(reinterpret_cast<const uint4*>(p.v_new + (size_t)b * row_elems) + v);
   uint8_t* vpage = p.v_pages + (size_t)page * p.v_page_stride;
   if (mode == EKV_MODE_TARGET_FP16) {
     reinterpret_cast<uint4*>(vpage + (size_t)row * row_elems * 2)[v] = vx;
@@ -461,10 +471,6 @@ append_kernel(const AppendParams p) {
     *dst = make_uint2(__byte_perm(vx.x, vx.y, 0x7531), __byte_perm(vx.z, vx.w, 0x7531));
     return;
   }
-  const int head = (8 * v) / p.D;
-  const float s = !p.v_scales ? 0.f
-                  : (p.scale_mode == EKV_SCALE_PER_TENSOR ? __ldg(p.v_scales)
-                                                           : __ldg(p.v_scales + (size_t)page * p.Hkv + head));
   if (!scale_ok(s)) {
     report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_SCALE, b);
     return;
