@@ -158,3 +158,27 @@ def test_prompt_longer_than_max_len_is_reported(ekv_lib, torch_cuda, variant):
     ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
     _check(out, lse, ref_out, ref_lse, np.arange(40 + 64))   # the short prompt whole, the long one's first 64
     assert np.all(np.isnan(out[40 + 64:]))                    # its later rows untouched
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_explicit_scale_empty_prompts_and_no_lse(ekv_lib, torch_cuda, variant):
+    torch = torch_cuda
+    lens = [0, 37, 0, 130, 1]
+    H_q, H_kv, D = 8, 2, 128
+    rng = np.random.default_rng(160)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    npages = [(l + 15) // 16 for l in lens]
+    po = np.concatenate([[0], np.cumsum(npages)[:-1]]).astype(np.int32)
+    W = sum(npages)
+    q = rng.standard_normal((int(cu[-1]), H_q, D)).astype(np.float16)
+    k = rng.standard_normal((W, 16, H_kv, D)).astype(np.float16)
+    v = rng.standard_normal((W, 16, H_kv, D)).astype(np.float16)
+    ctx = ekv_lib.Context(H_q, H_kv, D, 1, variant=variant)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    out = torch.full((q.shape[0], H_q, D), float("nan"), dtype=torch.float16, device="cuda")
+    ekv_lib.ekv_prefill_attention(ctx.handle, t(q), t(k), t(v), W, t(cu), t(po), len(lens), max(lens), 0.07, out, None)
+    torch.cuda.synchronize()
+    assert ctx.error() == (0, 0)
+    ref_out, _ = op.prefill_attention(q, k, v, cu, po, sm_scale=0.07)
+    e = np.abs(out.float().cpu().numpy() - ref_out).max()
+    assert e <= OUT_ATOL, f"max-abs error {e:.3e}"
