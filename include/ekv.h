@@ -365,6 +365,24 @@ ekv_status ekv_profile_read(ekv_ctx* ctx, double* split_ms, long long* launches)
  * compute the same function; 1 exists for measurement. */
 ekv_status ekv_set_decode_variant(ekv_ctx* ctx, int variant);
 
+/* Programmatic dependent launch of the decode (CUDA's griddepcontrol, sm_90+), for
+ * a stream of back-to-back calls (one per layer). enable = 1: ekv_paged_decode and
+ * ekv_paged_decode_elastic (decode variant 0) are launched with programmatic stream
+ * serialization and signal their own dependents at kernel start, so the next call's
+ * prologue and first page fills run on SMs as this call's CTAs leave, overlapping its
+ * merge tail. Ordering contract with the kernel immediately before the decode in the
+ * stream: before its grid-dependency wait the decode reads seq_lens, the block tables,
+ * page_mode, v_scales, boundaries and the K/V pages that are not the last page of
+ * their sequence; it reads q and writes out, lse and its workspace only after the
+ * preceding kernel has completed and its writes are visible. The preceding kernel may
+ * therefore write q and the last page of each sequence (ekv_append_kv does exactly
+ * that) but none of the other inputs. Kernels of this library never signal early
+ * except the decode itself, which writes no decode input. With a preceding kernel
+ * that does not signal (any other kernel, a copy, an event wait) nothing overlaps.
+ * enable = 0 (default): ordinary stream order. Returns EKV_ERR_INVALID_ARG for a
+ * null context or another value. */
+ekv_status ekv_set_pdl(ekv_ctx* ctx, int enable);
+
 /* Number of SMs and split-K CTAs per decode launch the context uses. */
 ekv_status ekv_query(ekv_ctx* ctx, int* num_sms, int* split_ctas);
 

@@ -38,6 +38,15 @@ __device__ __forceinline__ void report_error(int* err, int code, int detail, int
 }
 
 // ----------------------------------------------------------------------- mbarriers
+// Programmatic dependent launch (sm_90+). launch_dependents lets the next kernel of the
+// stream, when it was launched with programmatic serialization, be scheduled once every
+// CTA of this grid has executed it; wait blocks until the preceding grid has completed
+// and its memory operations are visible (it returns at once when there is none).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                : "memory");

@@ -57,6 +57,11 @@ struct DecodeParams {
   const int32_t* boundaries;      // [B][2] TARGET-BASE-TARGET boundaries, or null
   int num_v_slots;                // value slots (locations 0 .. 2*num_v_slots-1)
   int elastic;                    // 1: values read through v_block_table
+  // 1: launched with programmatic serialization (tensor-core consumer only). Before its
+  // griddepcontrol.wait the kernel reads only seq_lens, the block tables, page metadata
+  // and the K/V pages that are not the last page of their sequence; q is read and every
+  // output, record and ticket written after it.
+  int pdl;
 };
 
 constexpr int kMetaCompact = 1;   // E4M3 value page

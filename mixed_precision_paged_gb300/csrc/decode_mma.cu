@@ -122,16 +122,23 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
   wm_ids<EL>(p, cu, start, n_my, lane, cur);
   wm_ids<EL>(p, cu, start, n_my, 32 + lane, nxt);
   wm_meta<VMODE, EL>(p, tensor_scale, h, cur);
-  {
-    const int n0 = min(ring.nsl, n_my);              // prime the ring
-    for (int kk = 0; kk < n0; ++kk)
-      ring_issue<D, VMODE>(ring, kk, h, __shfl_sync(0xffffffffu, cur.page, kk),
-                           EL == kElYes ? __shfl_sync(0xffffffffu, cur.vloc, kk) : __shfl_sync(0xffffffffu, cur.page, kk),
-                           __shfl_sync(0xffffffffu, cur.flags, kk),
-                           EL == kElYes, tmK, tmV8, tmV16);
-  }
+  // prime the ring; under a programmatic launch the fills before the wait stop at the
+  // first page that is the last of its sequence (the cache writer, when it is the
+  // preceding kernel, is writing that page's new token row)
+  const int n0 = min(ring.nsl, n_my);
+  const int n_pre = p.pdl ? min(n0, cu[b_first + 1] - 1 - start) : n0;
+  auto prime = [&](int kk) {
+    ring_issue<D, VMODE>(ring, kk, h, __shfl_sync(0xffffffffu, cur.page, kk),
+                         EL == kElYes ? __shfl_sync(0xffffffffu, cur.vloc, kk) : __shfl_sync(0xffffffffu, cur.page, kk),
+                         __shfl_sync(0xffffffffu, cur.flags, kk), EL == kElYes, tmK, tmV8, tmV16);
+  };
+  for (int kk = 0; kk < n_pre; ++kk) prime(kk);
   wm_meta<VMODE, EL>(p, tensor_scale, h, nxt);
   wm_ids<EL>(p, cu, start, n_my, 64 + lane, nxt2);
+  if (p.pdl) {
+    griddep_wait();
+    for (int kk = n_pre; kk < n0; ++kk) prime(kk);
+  }
   int k = 0;                                        // next page of this warp
   bool timed_out = false;
 
@@ -380,6 +387,7 @@ decode_split_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   __shared__ int warp_tot[kThreads / 32];
   uint8_t* smem = aligned_smem(smem_raw);
   int start, end, per, b_first, b_last;
+  if (p.pdl) griddep_launch_dependents();          // the next call may take this SM when it frees
   if (!split_prologue(p, smem, warp_tot, start, end, per, b_first, b_last)) return;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmK);
@@ -395,8 +403,21 @@ static cudaError_t launch_mma(const CUtensorMap& tk, const CUtensorMap& t8, cons
   auto kern = decode_split_mma<D, VMODE, EL>;
   cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, st>>>(tk, t8, t16, p);
-  return cudaGetLastError();
+  if (!p.pdl) {
+    kern<<<grid, kThreads, smem, st>>>(tk, t8, t16, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, t8, t16, p);
 }
 
 template <int D>

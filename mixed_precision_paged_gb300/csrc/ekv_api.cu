@@ -29,6 +29,7 @@ struct ekv_ctx {
   ekv_config cfg{};
   int NG = 1;
   int variant = 0;            // 0 tensor-core consumer, 1 CUDA-core consumer
+  int pdl = 0;                // 1: decode launched with programmatic serialization
   float* part_acc = nullptr;
   float2* part_ml = nullptr;
   int* plan = nullptr;
@@ -134,6 +135,12 @@ ekv_status ekv_set_decode_variant(ekv_ctx* c, int variant) {
   return EKV_OK;
 }
 
+ekv_status ekv_set_pdl(ekv_ctx* c, int enable) {
+  if (!c || (enable != 0 && enable != 1)) return EKV_ERR_INVALID_ARG;
+  c->pdl = enable;
+  return EKV_OK;
+}
+
 namespace {
 
 // Shared body of the plain and the elastic decode. Elastic: v_block_table != null
@@ -199,6 +206,7 @@ ekv_status decode_impl(ekv_ctx* c, const void* q, const void* k_pages, const voi
   p.boundaries = elastic ? boundaries : nullptr;
   p.num_v_slots = elastic ? num_v_slots : num_pages;
   p.elastic = elastic ? 1 : 0;
+  p.pdl = c->pdl && c->variant == 0 ? 1 : 0;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   c->last_stream = st;

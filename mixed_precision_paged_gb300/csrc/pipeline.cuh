@@ -280,7 +280,14 @@ __device__ __forceinline__ bool split_prologue(const DecodeParams& p, uint8_t* s
   const int nv = (int)gridDim.x * p.NG;                // ranges: one per (CTA, page group)
   const int vtotal = total + kSegmentCost * p.batch;
   per = total > 0 ? (vtotal + nv - 1) / nv : 1;
-  if (blockIdx.x == 0) write_empty_sequences(p, cu);
+  if (blockIdx.x == 0) {
+    int mine = 0;
+    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) mine |= cu[b + 1] == cu[b];
+    if (__syncthreads_or(mine)) {
+      if (p.pdl) griddep_wait();                     // outputs only after the preceding kernel
+      write_empty_sequences(p, cu);
+    }
+  }
   if (total == 0 || (int)blockIdx.x * p.NG * per >= vtotal) return false;   // the whole CTA is idle
   for (int i = threadIdx.x; i < kWarps * p.nsl; i += blockDim.x) {
     mbar_init(reinterpret_cast<uint64_t*>(smem + p.bar_off) + i, 1);

@@ -48,7 +48,7 @@ EXPORTED = ["ekv_create", "ekv_destroy", "ekv_paged_decode", "ekv_gather_prefill
             "ekv_set_decode_variant", "ekv_query", "ekv_paged_decode_noalloc",
             "ekv_demote_pages_base", "ekv_promote_pages", "ekv_append_kv", "ekv_paged_decode_elastic",
             "ekv_transition_pages", "ekv_prefill_attention", "ekv_gather_prefill_elastic",
-            "ekv_status_string"]
+            "ekv_set_pdl", "ekv_status_string"]
 
 
 class ekv_config(ctypes.Structure):
@@ -82,6 +82,7 @@ _lib.ekv_get_error.argtypes = [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]
 _lib.ekv_profile_enable.argtypes = [_vp, _i]
 _lib.ekv_profile_read.argtypes = [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_ll)]
 _lib.ekv_set_decode_variant.argtypes = [_vp, _i]
+_lib.ekv_set_pdl.argtypes = [_vp, _i]
 _lib.ekv_query.argtypes = [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]
 _lib.ekv_status_string.argtypes = [_i]
 _lib.ekv_status_string.restype = ctypes.c_char_p
@@ -269,6 +270,10 @@ def ekv_set_decode_variant(ctx, variant):
     _check(_lib.ekv_set_decode_variant(ctx, variant), "ekv_set_decode_variant")
 
 
+def ekv_set_pdl(ctx, enable):
+    _check(_lib.ekv_set_pdl(ctx, int(enable)), "ekv_set_pdl")
+
+
 def ekv_query(ctx):
     a, b = _i(0), _i(0)
     _check(_lib.ekv_query(ctx, ctypes.byref(a), ctypes.byref(b)), "ekv_query")
@@ -284,11 +289,13 @@ def raw_status(fn_name, *args):
 class Context:
     """Owns one ekv context; methods take torch tensors and the case's metadata."""
 
-    def __init__(self, num_q_heads, num_kv_heads, head_dim, max_batch, variant=0):
+    def __init__(self, num_q_heads, num_kv_heads, head_dim, max_batch, variant=0, pdl=False):
         self.handle = ekv_create(num_q_heads, num_kv_heads, head_dim, max_batch)
         self.num_q_heads, self.num_kv_heads, self.head_dim = num_q_heads, num_kv_heads, head_dim
         if variant:
             ekv_set_decode_variant(self.handle, variant)
+        if pdl:
+            ekv_set_pdl(self.handle, 1)
 
     def close(self):
         if self.handle:

@@ -114,6 +114,43 @@ def test_many_short_sequences(ekv_lib, torch_cuda, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("hkv", [1, 8])
+def test_ranges_over_empty_sequences(ekv_lib, torch_cuda, variant, hkv):
+    # every sequence, empty ones included, weighs a fixed cost in the page stream that is cut
+    # into equal ranges, so with hundreds of empty and one-token sequences whole ranges hold
+    # no page at all, and one long sequence at the end is still split over many ranges
+    rng = np.random.default_rng(30 + hkv)
+    lens = [int(x) for x in rng.choice([0, 0, 0, 1, 2], size=700)] + [3000]
+    lens[350] = 0
+    case = wl.make_decode_case(lens, 8 * hkv, hkv, 128, v_format="mixed", scale_mode=1,
+                               pool_pages=sum((l + 15) // 16 for l in lens) + 2, seed=40 + hkv,
+                               p_base=0.25)
+    ctx = make_ctx(ekv_lib, case, variant)
+    out, lse = gpu_decode(ctx, to_device(case))
+    ref_out, ref_lse = oracle_decode(case)
+    assert_close(out, lse, ref_out, ref_lse)
+    empty = np.array(lens) == 0
+    assert np.all(out.float().cpu().numpy()[empty] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[empty]))
+    assert ctx.error() == (0, 0)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_batch_larger_than_the_range_count(ekv_lib, torch_cuda, variant):
+    # 1,200 short sequences with 8 KV heads: fewer ranges than sequences, so each range
+    # holds many whole sequences and writes them without a merge
+    rng = np.random.default_rng(33)
+    lens = [int(x) for x in rng.integers(0, 50, size=1200)]
+    case = wl.make_decode_case(lens, 16, 8, 64, v_format="mixed", scale_mode=0,
+                               pool_pages=sum((l + 15) // 16 for l in lens) + 2, seed=34)
+    ctx = make_ctx(ekv_lib, case, variant)
+    out, lse = gpu_decode(ctx, to_device(case))
+    ref_out, ref_lse = oracle_decode(case)
+    assert_close(out, lse, ref_out, ref_lse)
+    assert ctx.error() == (0, 0)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 def test_single_token_returns_value_times_scale(ekv_lib, torch_cuda, variant):
     case = wl.make_decode_case([1, 1, 1], 16, 4, 128, v_format="mixed", scale_mode=1,
                                pool_pages=6, seed=11)
