@@ -311,7 +311,10 @@ def config_of(args, wk):
                           "mixed": "K fp16 / V per page fp16 or e4m3 (p=0.5), per-(page, head) scale"}[wk["v_format"]],
             "l2": "inputs larger than L2: distinct layer pools streamed in turn"
                   if (args.layers or wk["layers"]) > 1 else "L2 flushed (1 GiB read) between steps",
-            "parallelism": f"dp{args.gpus} (independent batches per GPU, no collective)"}
+            "parallelism": f"dp{args.gpus} (independent batches per GPU, no collective)",
+            "launch": ("programmatic dependent launch: each layer call's prologue and first page fills "
+                       "overlap the previous call's tail" if args.pdl and args.variant == 0
+                       else "plain stream order")}
 
 
 # ---------------------------------------------------------------------- companions
@@ -534,6 +537,8 @@ def main():
     ap.add_argument("--workload", default="pages_shape", choices=sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--variant", type=int, default=0, help="0 tensor-core, 1 CUDA-core consumer")
+    ap.add_argument("--pdl", type=int, default=1, choices=[0, 1],
+                    help="programmatic dependent launch between the layer calls (tensor-core consumer)")
     ap.add_argument("--seed", type=int, default=1002)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-companions", action="store_true")
@@ -588,7 +593,8 @@ def main():
     step_bytes = sum(x["total"] for x in per_call)
     split_bytes = float(np.mean([x["split"] for x in per_call]))
 
-    ctx = ekv.Context(Hq, Hkv, D, B, variant=args.variant)
+    pdl = bool(args.pdl) and args.variant == 0
+    ctx = ekv.Context(Hq, Hkv, D, B, variant=args.variant, pdl=pdl)
     outs = [torch.empty((B, Hq, D), dtype=torch.float16, device="cuda") for _ in range(layers)]
     stream = torch.cuda.current_stream()
     # one-layer runs evict L2 between steps by reading 1 GiB (a read leaves no dirty
@@ -632,7 +638,9 @@ def main():
         torch.cuda.synchronize()
         elapsed_ms -= f0.elapsed_time(f1)
     # the split kernel's own duration for the roofline: a separate pass with the library's
-    # CUDA events around each split launch (kept out of the timed region above)
+    # CUDA events around each split launch (kept out of the timed region above), each
+    # launch in plain stream order so that its events bracket it alone
+    ekv.ekv_set_pdl(ctx.handle, 0)
     ekv.ekv_profile_enable(ctx.handle, True)
     ekv.ekv_profile_read(ctx.handle)
     for _ in range(min(args.steps, 20)):
@@ -640,6 +648,7 @@ def main():
     torch.cuda.synchronize()
     split_ms, split_n = ekv.ekv_profile_read(ctx.handle)
     ekv.ekv_profile_enable(ctx.handle, False)
+    ekv.ekv_set_pdl(ctx.handle, int(pdl))
     err = ctx.error()
     if world > 1:
         t = torch.tensor([elapsed_ms], device="cuda")
@@ -647,46 +656,61 @@ def main():
         elapsed_ms = float(t.item())
 
     # end to end through the C ABI: per-step inputs from pinned host memory, outputs back.
-    # Each layer's inputs (q, block table, seq_lens) are one contiguous pinned buffer and one
-    # H2D copy on a copy stream, and each layer's output goes back on that stream while the
-    # next layer decodes; events order every copy against the kernels that use it.
-    def packed(c):
-        parts = [c.q.contiguous().view(torch.uint8).reshape(-1), c.block_table.contiguous().view(torch.uint8).reshape(-1),
-                 c.seq_lens.contiguous().view(torch.uint8).reshape(-1)]
+    # The layers go in chunks (a first chunk of one layer, then up to seven): each chunk's
+    # inputs (q, block tables, seq_lens of its layers) are one contiguous pinned buffer and
+    # one H2D copy on a copy stream, and each chunk's outputs go back in one copy on that
+    # stream while the next chunk decodes. Events order every copy against the kernels that
+    # use it; inside a chunk the layer calls follow each other directly in the stream.
+    bounds = [0, 1] + list(range(8, layers, 7)) + [layers] if layers > 1 else [0, 1]
+    chunks = [list(range(a, b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+
+    def packed(ls):
+        parts = []
+        for l in ls:
+            c = cases[l]
+            parts += [c.q.contiguous().view(torch.uint8).reshape(-1),
+                      c.block_table.contiguous().view(torch.uint8).reshape(-1),
+                      c.seq_lens.contiguous().view(torch.uint8).reshape(-1)]
         return torch.cat(parts).cpu().pin_memory(), [p.numel() for p in parts]
-    in_h, sizes = zip(*[packed(c) for c in cases])
+    in_h, sizes = zip(*[packed(ls) for ls in chunks])
     in_d = [torch.empty_like(h, device="cuda") for h in in_h]
-    views = []
-    for l, c in enumerate(cases):
-        nq, nbt, _ = sizes[l]
-        views.append((in_d[l][:nq].view(torch.float16).view(c.q.shape),
-                      in_d[l][nq:nq + nbt].view(torch.int32).view(c.block_table.shape),
-                      in_d[l][nq + nbt:].view(torch.int32)))
-    out_h = [torch.empty((B, Hq, D), dtype=torch.float16).pin_memory() for _ in range(layers)]
+    views = {}
+    for ci, ls in enumerate(chunks):
+        off = 0
+        for i, l in enumerate(ls):
+            nq, nbt, nsl = sizes[ci][3 * i:3 * i + 3]
+            c = cases[l]
+            views[l] = (in_d[ci][off:off + nq].view(torch.float16).view(c.q.shape),
+                        in_d[ci][off + nq:off + nq + nbt].view(torch.int32).view(c.block_table.shape),
+                        in_d[ci][off + nq + nbt:off + nq + nbt + nsl].view(torch.int32))
+            off += nq + nbt + nsl
+    out_d = [torch.empty((len(ls), B, Hq, D), dtype=torch.float16, device="cuda") for ls in chunks]
+    out_h = [torch.empty((len(ls), B, Hq, D), dtype=torch.float16).pin_memory() for ls in chunks]
     h2d = sum(h.numel() for h in in_h)
     d2h = sum(o.numel() * 2 for o in out_h)
     copy = torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(layers)]
-    ev_out = [torch.cuda.Event() for _ in range(layers)]
+    ev_in = [torch.cuda.Event() for _ in chunks]
+    ev_out = [torch.cuda.Event() for _ in chunks]
     ev_done = torch.cuda.Event()
 
     def e2e_step():
         copy.wait_stream(stream)                     # the previous step's kernels have used the buffers
-        for l in range(layers):
+        for ci in range(len(chunks)):
             with torch.cuda.stream(copy):
-                in_d[l].copy_(in_h[l], non_blocking=True)
-                ev_in[l].record(copy)
-        for l in range(layers):
-            stream.wait_event(ev_in[l])
-            c = cases[l]
-            q_l, bt_l, sl_l = views[l]
-            ekv.ekv_paged_decode(ctx.handle, q_l, c.k_pages, c.v_pages, c.v_page_stride, c.num_pages,
-                                 c.v_scales, c.scale_mode, c.page_mode, c.uniform_mode, bt_l,
-                                 int(c.block_table.shape[1]), sl_l, B, 0.0, outs[l], None, stream)
-            ev_out[l].record(stream)
-            copy.wait_event(ev_out[l])
+                in_d[ci].copy_(in_h[ci], non_blocking=True)
+                ev_in[ci].record(copy)
+        for ci, ls in enumerate(chunks):
+            stream.wait_event(ev_in[ci])
+            for i, l in enumerate(ls):
+                c = cases[l]
+                q_l, bt_l, sl_l = views[l]
+                ekv.ekv_paged_decode(ctx.handle, q_l, c.k_pages, c.v_pages, c.v_page_stride, c.num_pages,
+                                     c.v_scales, c.scale_mode, c.page_mode, c.uniform_mode, bt_l,
+                                     int(c.block_table.shape[1]), sl_l, B, 0.0, out_d[ci][i], None, stream)
+            ev_out[ci].record(stream)
+            copy.wait_event(ev_out[ci])
             with torch.cuda.stream(copy):
-                out_h[l].copy_(outs[l], non_blocking=True)
+                out_h[ci].copy_(out_d[ci], non_blocking=True)
         ev_done.record(copy)
         stream.wait_event(ev_done)                   # the step ends when its last output is home
 
@@ -702,6 +726,9 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    # the outputs that came home equal the device-timed calls' outputs bit for bit
+    e2e_same = all(torch.equal(out_h[ci][i], outs[l].cpu()) for ci, ls in enumerate(chunks)
+                   for i, l in enumerate(ls))
     if world > 1:
         t = torch.tensor([e2e_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -728,7 +755,8 @@ def main():
                      "algorithmic_bytes_per_launch": split_bytes,
                      "avg_launch_ms": split_ms / split_n if split_n else None},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps},
+                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
+                "layer_chunks": [len(ls) for ls in chunks], "outputs_equal_device_run": e2e_same},
         "gpu_launches": layers * args.steps,
         "clocks": clock_rec,
         "kv_dtype": "K f16, V e4m3 (compact) / f16 (TARGET); f32 accumulation",

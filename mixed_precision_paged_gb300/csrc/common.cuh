@@ -38,6 +38,11 @@ __device__ __forceinline__ void report_error(int* err, int code, int detail, int
 }
 
 // ----------------------------------------------------------------------- mbarriers
+// Release/acquire fence at GPU scope: lighter than __threadfence (a sequentially
+// consistent fence); with a relaxed atomic after it (release) or before it (acquire) it
+// forms the message-passing pattern of the PTX memory model.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Programmatic dependent launch (sm_90+). launch_dependents lets the next kernel of the
 // stream, when it was launched with programmatic serialization, be scheduled once every
 // CTA of this grid has executed it; wait blocks until the preceding grid has completed

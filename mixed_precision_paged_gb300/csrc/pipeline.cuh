@@ -473,7 +473,8 @@ __device__ void finish_warp(const DecodeParams& p, const int* cu, int start, int
   __syncwarp();
   unsigned last_mask = 0;
   if (lane == 0 && n_cross > 0) {
-    __threadfence();                                   // this warp's records before its tickets
+    fence_acq_rel_gpu();                               // release: the warp's records (ordered
+                                                       // before lane 0 by the __syncwarp) first
     int old[2] = {0, 0};
     int* tk[2] = {nullptr, nullptr};
     for (int e = 0; e < n_cross; ++e) {
@@ -488,7 +489,8 @@ __device__ void finish_warp(const DecodeParams& p, const int* cu, int start, int
         *tk[e] = 0;
       }
     }
-    if (last_mask) __threadfence();                    // other warps' records after their tickets
+    if (last_mask) fence_acq_rel_gpu();                // acquire: the other ranges' records; the
+                                                       // merge's __syncwarp orders the lanes' loads after it
   }
   last_mask = __shfl_sync(0xffffffffu, last_mask, 0);
   MergeJob jobs[2];
