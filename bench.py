@@ -72,7 +72,7 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ["decode_mma.cu", "pipeline.cuh", "decode.cuh", "common.cuh", "pool_maps.h"]:
+    for f in ["decode_mma.cu", "pipeline.cuh", "decode.cuh", "common.cuh", "pool_maps.h", "decode_simt.cu"]:
         h.update(open(os.path.join(ROOT, "mixed_precision_paged_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -237,17 +237,16 @@ __device__ __forceinline__ MergeBuf merge_buf(const WarpRing& ring, int slot_byt
   return mb;
 }
 
-// Fill the ring slot of page k (metadata page/flags broadcast by the caller). Lane 0
-// arms the slot's barrier with the slice's bytes and issues one bulk tensor copy per
-// tensor: K through the 5-D fp16 slice map, V through the byte map (E4M3 or BASE page)
-// or the fp16 slice map (TARGET page). A skipped page only arrives on the barrier.
+// Fill ring slot s with page k (metadata page/flags broadcast by the caller; s = k mod
+// nsl), from lane 0: arm the slot's barrier with the slice's bytes and issue one bulk
+// tensor copy per tensor: K through the 5-D fp16 slice map, V through the byte map (E4M3
+// or BASE page) or the fp16 slice map (TARGET page). A skipped page only arrives on the
+// barrier.
 template <int D, int VMODE>
-__device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, int page, int vloc, int flags,
-                                           bool elastic, const CUtensorMap* tmK, const CUtensorMap* tmV8,
-                                           const CUtensorMap* tmV16) {
+__device__ __forceinline__ void ring_fill(const WarpRing& ring, int s, int h, int page, int vloc, int flags,
+                                          bool elastic, const CUtensorMap* tmK, const CUtensorMap* tmV8,
+                                          const CUtensorMap* tmV16) {
   using S = Slot<D, VMODE>;
-  if ((threadIdx.x & 31) != 0) return;
-  const int s = k % ring.nsl;
   uint64_t* bar = &ring.full[s];
   if (flags & kMetaSkip) {
     mbar_arrive(bar);
@@ -265,6 +264,24 @@ __device__ __forceinline__ void ring_issue(const WarpRing& ring, int k, int h, i
     if (compact) tma_load_4d(dst + S::kK, tmV8, 0, h, 0, vloc, bar);
     else tma_load_5d(dst + S::kK, tmV16, 0, 0, 0, h, vloc, bar);
   }
+}
+
+// ring_fill of slot s from the warp (lanes other than 0 return).
+template <int D, int VMODE>
+__device__ __forceinline__ void ring_issue(const WarpRing& ring, int s, int h, int page, int vloc, int flags,
+                                           bool elastic, const CUtensorMap* tmK, const CUtensorMap* tmV8,
+                                           const CUtensorMap* tmV16) {
+  if ((threadIdx.x & 31) != 0) return;
+  ring_fill<D, VMODE>(ring, s, h, page, vloc, flags, elastic, tmK, tmV8, tmV16);
+}
+
+// ring_fill of page k's slot (k mod nsl, computed by lane 0 alone).
+template <int D, int VMODE>
+__device__ __forceinline__ void ring_issue_page(const WarpRing& ring, int k, int h, int page, int vloc, int flags,
+                                                bool elastic, const CUtensorMap* tmK, const CUtensorMap* tmV8,
+                                                const CUtensorMap* tmV16) {
+  if ((threadIdx.x & 31) != 0) return;
+  ring_fill<D, VMODE>(ring, k % ring.nsl, h, page, vloc, flags, elastic, tmK, tmV8, tmV16);
 }
 
 
