@@ -98,12 +98,11 @@ constexpr float kRebase = 8.f;
 
 // Two orders of the per-page steps, chosen per pool by measurement (the per-page chain is
 // latency-bound, and its instruction order moves the stream rate by several percent):
-//  consume_mma_late (uniform E4M3 pool): loads, QK, sums, V conversion, refill of the
-//    slot, page max reduced over the warp on every page;
+//  consume_mma_late (uniform E4M3 pool): loads, QK, sums, V conversion, refill of the slot;
 //  consume_mma (FP16, mixed and elastic pools): loads, QK issued, refill, sums and
-//    conversion, lazy re-base of the running max.
-// Per layer on the same box: the second order gives mixed +10%, TARGET/BASE +11%, FP16
-// +1.5%, and uniform E4M3 -2.4%, so E4M3 keeps the first.
+//    conversion.
+// Both re-base the running max lazily. Per layer on the same box the second order gives
+// mixed +10%, TARGET/BASE +11%, FP16 +1.5%, and uniform E4M3 -2.4%, so E4M3 keeps the first.
 template <int D, int VMODE, int EL>
 __device__ void consume_mma_late(const DecodeParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV8,
                             const CUtensorMap* tmV16, uint8_t* smem, int start, int end, int b_first,
@@ -285,16 +284,15 @@ __device__ void consume_mma_late(const DecodeParams& p, const CUtensorMap* tmK, 
         const float s01 = v_lo ? sc[1] * p.qscale : -INFINITY;
         const float s10 = v_hi ? sc[2] * p.qscale : -INFINITY;
         const float s11 = v_hi ? sc[3] * p.qscale : -INFINITY;
+        // running max re-based lazily, as in consume_mma
         float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+        if (__any_sync(0xffffffffu, (mx0 > m0 + kRebase) || (mx1 > m1 + kRebase))) {
 #pragma unroll
-        for (int o = 4; o <= 16; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const __half2 plo = __floats2half2_rn(ex2(s00 - mn0), ex2(s01 - mn1));   // token r8
-        const __half2 phi = __floats2half2_rn(ex2(s10 - mn0), ex2(s11 - mn1));   // token r8+8
-        if (__any_sync(0xffffffffu, (mn0 > m0) || (mn1 > m1))) {
+          for (int o = 4; o <= 16; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+          }
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
           const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
           l0 *= al0;
           l1 *= al1;
@@ -306,6 +304,8 @@ __device__ void consume_mma_late(const DecodeParams& p, const CUtensorMap* tmK, 
           m0 = mn0;
           m1 = mn1;
         }
+        const __half2 plo = __floats2half2_rn(ex2(s00 - m0), ex2(s01 - m1));   // token r8
+        const __half2 phi = __floats2half2_rn(ex2(s10 - m0), ex2(s11 - m1));   // token r8+8
         {
           const float2 a = __half22float2(plo), c = __half22float2(phi);
           l0 += a.x + c.x;

@@ -151,6 +151,47 @@ def test_batch_larger_than_the_range_count(ekv_lib, torch_cuda, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("fmt,scale_mode", [("fp16", 0), ("mixed", 1), ("e4m3", 0)])
+def test_scores_growing_along_the_sequence(ekv_lib, torch_cuda, variant, fmt, scale_mode):
+    # keys scaled up page by page, so the page max of the scores keeps passing the running
+    # reference and the lazy re-base (FP16 / mixed pools) fires every few pages, mid-segment
+    lens = [900, 37, 1600]
+    case = wl.make_decode_case(lens, 32, 8, 128, v_format=fmt, scale_mode=scale_mode,
+                               pool_pages=sum((l + 15) // 16 for l in lens) + 3, seed=60,
+                               p_base=0.25 if fmt == "mixed" else 0.0)
+    k = case.k_pages.astype(np.float32)
+    for b, L in enumerate(lens):
+        for j in range((L + 15) // 16):
+            k[case.block_table[b, j]] *= 1.0 + 0.25 * j
+    case.k_pages = k.astype(np.float16)
+    ctx = make_ctx(ekv_lib, case, variant)
+    out, lse = gpu_decode(ctx, to_device(case))
+    ref_out, ref_lse = oracle_decode(case)
+    assert_close(out, lse, ref_out, ref_lse)
+    assert ctx.error() == (0, 0)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("fmt", ["fp16", "mixed"])
+def test_one_late_dominant_token(ekv_lib, torch_cuda, variant, fmt):
+    # one key far along the sequence aligned with the query: its score is ~40 (log2 units)
+    # above the rest, so the reference jumps once by far more than the re-base threshold and
+    # the output is essentially that token's value
+    lens = [700, 333]
+    case = wl.make_decode_case(lens, 8, 2, 128, v_format=fmt, scale_mode=1, seed=61,
+                               pool_pages=sum((l + 15) // 16 for l in lens) + 3)
+    for b, t in [(0, 650), (1, 100)]:
+        page, row = case.block_table[b, t // 16], t % 16
+        for hk in range(2):
+            qd = case.q[b, hk * 4].astype(np.float32)
+            case.k_pages[page, row, hk] = (qd * (30.0 / np.linalg.norm(qd))).astype(np.float16)
+    ctx = make_ctx(ekv_lib, case, variant)
+    out, lse = gpu_decode(ctx, to_device(case))
+    ref_out, ref_lse = oracle_decode(case)
+    assert_close(out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 def test_single_token_returns_value_times_scale(ekv_lib, torch_cuda, variant):
     case = wl.make_decode_case([1, 1, 1], 16, 4, 128, v_format="mixed", scale_mode=1,
                                pool_pages=6, seed=11)
