@@ -43,6 +43,8 @@ def test_null_arguments_are_rejected_without_a_gpu(ekv_lib):
     assert L.ekv_paged_decode(None, *([None] * 3), 0, 0, None, 0, None, 0, None, 0, None, 1,
                               ctypes.c_float(0), None, None, None) == ekv_lib.EKV_ERR_INVALID_ARG
     assert L.ekv_demote_pages(None, None, 0, 0, None, 0, None, None, None) == ekv_lib.EKV_ERR_INVALID_ARG
+    assert L.ekv_set_pdl(None, 1) == ekv_lib.EKV_ERR_INVALID_ARG
+    assert L.ekv_set_decode_variant(None, 0) == ekv_lib.EKV_ERR_INVALID_ARG
     assert L.ekv_destroy(None) == ekv_lib.EKV_OK
 
 

@@ -135,3 +135,24 @@ def test_programmatic_edges_in_a_cuda_graph(ekv_lib, torch_cuda):
         for c, o, l in zip(layers, outs, lses):
             ro, rl = oracle_decode(c)
             assert_close(o, l, ro, rl)
+
+
+def test_switch_values_and_the_cuda_core_consumer(ekv_lib, torch_cuda):
+    # the switch takes 0 or 1 only; the CUDA-core consumer (variant 1) ignores it and runs
+    # in plain stream order with the same results
+    torch = torch_cuda
+    ctx = ekv_lib.Context(32, 8, 128, 4, variant=1, pdl=True)
+    assert ekv_lib.raw_status("ekv_set_pdl", ctx.handle, 2) == ekv_lib.EKV_ERR_INVALID_ARG
+    lens = [300, 0, 17, 1000]
+    case = wl.make_decode_case(lens, 32, 8, 128, v_format="mixed", scale_mode=1, seed=800,
+                               pool_pages=sum((x + 15) // 16 for x in lens) + 3)
+    dv = to_device(case)
+    out = torch.empty((4, 32, 128), dtype=torch.float16, device="cuda")
+    lse = torch.empty((4, 32), dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        ctx.decode(dv, out, lse)
+    torch.cuda.synchronize()
+    assert ctx.error() == (0, 0)
+    ro, rl = oracle_decode(case)
+    assert_close(out, lse, ro, rl)
+
