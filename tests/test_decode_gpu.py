@@ -191,6 +191,31 @@ def test_one_late_dominant_token(ekv_lib, torch_cuda, variant, fmt):
     assert_close(out, lse, ref_out, ref_lse)
 
 
+@pytest.fixture(scope="module")
+def max_batch_case():
+    rng = np.random.default_rng(35)
+    lens = [int(x) for x in rng.integers(0, 40, size=4096)]
+    return lens, wl.make_decode_case(lens, 32, 8, 128, v_format="mixed", scale_mode=1, seed=36,
+                                     pool_pages=sum((l + 15) // 16 for l in lens) + 2, p_base=0.2)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_maximum_batch(ekv_lib, torch_cuda, variant, max_batch_case):
+    # the largest batch a context takes (4,096 sequences: the prefix sums fill 16 KiB of
+    # shared memory beside FP16-sized ring slots), short mixed-pool sequences, some empty;
+    # sampled sequences against the oracle, every empty one checked for zeros
+    lens, case = max_batch_case
+    ctx = make_ctx(ekv_lib, case, variant)
+    out, lse = gpu_decode(ctx, to_device(case))
+    assert ctx.error() == (0, 0)
+    idx = np.concatenate([np.arange(0, 4096, 97), [4095]])
+    ref_out, ref_lse = oracle_decode(case, batch_indices=idx)
+    assert_close(out[idx], lse[idx], ref_out[idx], ref_lse[idx])
+    empty = np.array(lens) == 0
+    assert np.all(out.float().cpu().numpy()[empty] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[empty]))
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_single_token_returns_value_times_scale(ekv_lib, torch_cuda, variant):
     case = wl.make_decode_case([1, 1, 1], 16, 4, 128, v_format="mixed", scale_mode=1,
