@@ -14,6 +14,9 @@ e2e          the same metric through the C ABI with the per-step inputs (q, bloc
 roofline     split kernel's algorithmic bytes / its own event-timed duration, against
              the measured HBM copy peak
 cpu_baseline the float64 oracle on the host cores, on a sample of the same workload
+decode_workloads  the mixed-fidelity batch, its all-FP16 control, the TARGET/BASE mix
+             and high concurrency, each on its own pools (per layer under programmatic
+             launch, and per launch alone)
 companions   gather, demotion (E4M3, BASE), promotion, append and FP16 prefill on their
              workloads (32 x 8192-token prompts; 8 x 8192 for prefill)
 
@@ -70,29 +73,51 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+def _production_source(data):
+    """Source text as the production library compiles it: blocks that only the tests'
+    library builds (#ifdef EKV_TEST_WAIT_TIMEOUT ... #endif) are dropped with the blank
+    line after them; where such a block has an #else branch, that branch is kept."""
+    out, state, drop_blank = [], 0, False
+    for line in data.decode().splitlines(keepends=True):
+        if line.startswith("#ifdef EKV_TEST_WAIT_TIMEOUT"):
+            state = 1
+            continue
+        if state:
+            if line.startswith("#else"):
+                state = 2
+            elif line.startswith("#endif"):
+                state, drop_blank = 0, state == 1
+            elif state == 2:
+                out.append(line)
+            continue
+        if drop_blank and line.strip() == "":
+            drop_blank = False
+            continue
+        drop_blank = False
+        out.append(line)
+    return "".join(out).encode()
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ["decode_mma.cu", "pipeline.cuh", "decode.cuh", "common.cuh", "pool_maps.h", "decode_simt.cu"]:
-        h.update(open(os.path.join(ROOT, "mixed_precision_paged_gb300", "csrc", f), "rb").read())
+        h.update(_production_source(open(os.path.join(ROOT, "mixed_precision_paged_gb300", "csrc", f), "rb").read()))
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload):
-    """DRAM bytes per split launch from the committed ncu summary, when it was taken
-    on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"decode_split_mma_{workload}.md")
-    if not os.path.exists(path):
+    """DRAM bytes per split launch from profiles/traffic.json (written from the committed
+    ncu summaries), when it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))["decode_split_mma"][workload]
+    except (OSError, ValueError, KeyError):
         return None
-    vals = {}
-    for line in open(path):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_hash") != kernel_source_hash():
+    if rec.get("kernel_source_hash") != kernel_source_hash():
         return None
     try:
-        return float(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return float(rec["traffic_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -323,22 +348,16 @@ def companions(ekv, torch, peaks):
     """Gather (4 chunks of 8 prompts into a 4,096-page workspace) and demotion of 50% of
     16,384 FP16 value pages, on the 32 x 8192-token gather/demote workload."""
     from mixed_precision_paged_gb300 import roofline as rf
+    from mixed_precision_paged_gb300 import workloads as wl
     H, D, S = 8, 128, 16
-    P = 32 * 8192 // S
-    g = torch.Generator(device="cuda")
-    g.manual_seed(1004)
-    k = torch.randn((P, S, H, D), generator=g, device="cuda").to(torch.float16)
-    vv = torch.randn((P, S, H, D), generator=g, device="cuda")
-    a = vv.abs().amax(dim=(1, 3))
-    sc = torch.where(a > 0, a / 448.0, torch.ones_like(a)).contiguous()
-    v8 = (vv / sc[:, None, :, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).reshape(P, -1)
-    del vv
-    bt = torch.randperm(P, generator=g, device="cuda").to(torch.int32).reshape(32, 512)
-    ws_k = torch.empty((4096, S, H, D), dtype=torch.float16, device="cuda")
+    gd = wl.device_gather_demote_case(seed=1004)
+    P = gd.k_pages.shape[0]
+    k, v8, sc, bt = gd.k_pages, gd.v8_pages, gd.v_scales, gd.block_table
+    ws_k = torch.empty((gd.ws_pages, S, H, D), dtype=torch.float16, device="cuda")
     ws_v = torch.empty_like(ws_k)
-    idx = torch.empty((4096,), dtype=torch.int32, device="cuda")
+    idx = torch.empty((gd.ws_pages,), dtype=torch.int32, device="cuda")
     ctx = ekv.Context(H, H, D, 1)
-    chunks = [np.array([[s, 0, 512] for s in range(c * 8, c * 8 + 8)]) for c in range(4)]
+    chunks = gd.chunks
 
     def gather_all():
         for pr in chunks:
@@ -357,12 +376,13 @@ def companions(ekv, torch, peaks):
     t_g = s.elapsed_time(e) / reps
     gb = rf.gather_bytes(P, P, H, D, per_page_scales=True)
     # demotion: FP16 pool N(0, 2), half of the pages
-    v16 = (torch.randn((P, S, H, D), generator=g, device="cuda") * math.sqrt(2.0)).to(torch.float16)
-    v16b = v16.view(torch.uint8).reshape(P, -1)
+    v16b = gd.v16_pages
     work = torch.empty_like(v16b)
     mode = torch.zeros(P, dtype=torch.uint8, device="cuda")
     scale_out = torch.zeros((P, H), dtype=torch.float32, device="cuda")
-    ids = torch.randperm(P, generator=g, device="cuda")[: P // 2].to(torch.int32)
+    ids = gd.demote_ids
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1005)
     flush = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
     ts = []
     for rep in range(8):
@@ -488,6 +508,92 @@ def companions(ekv, torch, peaks):
     return out
 
 
+# ------------------------------------------------------------ other decode workloads
+
+def layer_bytes(wk, lens, cases):
+    """Algorithmic bytes of each layer call of a workload (roofline.decode_bytes)."""
+    from mixed_precision_paged_gb300 import roofline as rf
+    Hq, Hkv, D = wk["q_heads"], wk["kv_heads"], wk["head_dim"]
+    per_call = []
+    for c in cases:
+        if wk["v_format"] == "mixed":
+            modes = c.page_mode.cpu().numpy()
+            bt = c.block_table.cpu().numpy()
+            code = {0: 2, 1: 1, 2: -1}                  # TARGET, E4M3, BASE (see decode_bytes)
+            vbp = [[code[int(modes[bt[b, j]])] for j in range((l + 15) // 16)] for b, l in enumerate(lens)]
+            per_call.append(rf.decode_bytes(lens, Hq, Hkv, D, vbp, per_page_scales=True))
+        else:
+            per_call.append(rf.decode_bytes(lens, Hq, Hkv, D, 1 if wk["v_format"] == "e4m3" else 2,
+                                            per_page_scales=False))
+    return per_call
+
+
+def decode_workloads(ekv, torch, peaks, steps, warmup, seed):
+    """The other decode configurations, each on its own layer pools drawn with the seeds
+    the full-size parity tests check: the mixed-fidelity batch (p = 0.5 TARGET / E4M3),
+    its all-FP16 control, the TARGET / BASE mix (2 layers each, 3.8-4.4 GB per layer) and
+    high concurrency (48 layers, 51 GB). Per workload: the step of all layer calls under
+    programmatic dependent launch (us per layer, GB/s, tokens/s), and each call alone in
+    plain stream order (the library's per-launch events)."""
+    from mixed_precision_paged_gb300 import workloads as wl
+    hbm = float(peaks["hbm_gbs"])
+    res = {}
+    for name in ("mixed", "mixed_fp16_control", "mixed_base", "high_concurrency"):
+        wk = WORKLOADS[name]
+        lens = lens_for(name)
+        B, Hq, Hkv, D, layers = len(lens), wk["q_heads"], wk["kv_heads"], wk["head_dim"], wk["layers"]
+        cases = [wl.device_decode_case(lens, Hq, Hkv, D, v_format=wk["v_format"], scale_mode=wk["scale_mode"],
+                                       seed=seed + 7919 * l, p_compact=wk.get("p_compact", 0.5),
+                                       p_base=wk.get("p_base", 0.0)) for l in range(layers)]
+        per_call = layer_bytes(wk, lens, cases)
+        step_bytes = sum(x["total"] for x in per_call)
+        split_bytes = float(np.mean([x["split"] for x in per_call]))
+        ctx = ekv.Context(Hq, Hkv, D, B, pdl=True)
+        outs = [torch.empty((B, Hq, D), dtype=torch.float16, device="cuda") for _ in range(layers)]
+        stream = torch.cuda.current_stream()
+
+        def step():
+            for l in range(layers):
+                ctx.decode(cases[l], outs[l], stream=stream)
+        n_steps = max(steps, 10) if layers > 2 else max(steps, 20)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(n_steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        ms_step = t0.elapsed_time(t1) / n_steps
+        ekv.ekv_set_pdl(ctx.handle, 0)                   # each launch alone, between its events
+        ekv.ekv_profile_enable(ctx.handle, True)
+        ekv.ekv_profile_read(ctx.handle)
+        for _ in range(max(1, 40 // layers)):
+            step()
+        torch.cuda.synchronize()
+        split_ms, split_n = ekv.ekv_profile_read(ctx.handle)
+        err = ctx.error()
+        ctx.close()
+        gbs = step_bytes / (ms_step / 1e3) / 1e9
+        launch_ms = split_ms / split_n
+        res[name] = {
+            "workload": wk["desc"], "batch": B, "context": wk["context"], "q_heads": Hq, "kv_heads": Hkv,
+            "head_dim": D, "layers": layers, "kv_format": wk["v_format"], "steps": n_steps,
+            "us_per_layer": ms_step / layers * 1e3, "GB/s": gbs, "frac_of_measured_hbm": gbs / hbm,
+            "frac_of_8tbs_spec": gbs / 8000.0,
+            "tokens_per_s": B / (ms_step / 1e3) if layers > 2 else B / (ms_step / layers / 1e3),
+            "tokens_per_s_unit": (f"sequences / s, one step = {layers} layer calls" if layers > 2
+                                  else "sequences / s per layer call"),
+            "per_launch_plain_order": {"us": launch_ms * 1e3, "GB/s": split_bytes / (launch_ms / 1e3) / 1e9,
+                                       "frac_of_measured_hbm": split_bytes / (launch_ms / 1e3) / 1e9 / hbm},
+            "traffic_bytes_per_launch": profiled_traffic(name),
+            "device_error": list(err)}
+        del cases, outs
+        torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- main
 
 def run_prefill_only(args):
@@ -579,17 +685,7 @@ def main():
                                    p_base=wk.get("p_base", 0.0)) for l in range(layers)]
     torch.cuda.synchronize()
     # algorithmic bytes per layer call
-    per_call = []
-    for c in cases:
-        if wk["v_format"] == "mixed":
-            modes = c.page_mode.cpu().numpy()
-            bt = c.block_table.cpu().numpy()
-            code = {0: 2, 1: 1, 2: -1}                  # TARGET, E4M3, BASE (see decode_bytes)
-            vbp = [[code[int(modes[bt[b, j]])] for j in range((l + 15) // 16)] for b, l in enumerate(lens)]
-            per_call.append(rf.decode_bytes(lens, Hq, Hkv, D, vbp, per_page_scales=True))
-        else:
-            per_call.append(rf.decode_bytes(lens, Hq, Hkv, D, 1 if wk["v_format"] == "e4m3" else 2,
-                                            per_page_scales=False))
+    per_call = layer_bytes(wk, lens, cases)
     step_bytes = sum(x["total"] for x in per_call)
     split_bytes = float(np.mean([x["split"] for x in per_call]))
 
@@ -740,6 +836,10 @@ def main():
     e2e_value = step_bytes * args.e2e_steps * world / (e2e_ms / 1e3) / 1e9
     ms_step = elapsed_ms / args.steps
     achieved = split_bytes / (split_ms / split_n / 1e3) / 1e9 if split_n else None
+    # the same kernel inside the timed stream: each step is its layer calls alone, so the
+    # timed region divided by its launches is the kernel's time per launch in the stream
+    stream_ms = elapsed_ms / (args.steps * layers) if flush is None else None
+    stream_achieved = split_bytes / (stream_ms / 1e3) / 1e9 if stream_ms else None
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -753,7 +853,14 @@ def main():
                      "kernel": "decode_split_mma" if args.variant == 0 else "decode_split_simt",
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": split_bytes,
-                     "avg_launch_ms": split_ms / split_n if split_n else None},
+                     "avg_launch_ms": split_ms / split_n if split_n else None,
+                     "launch_mode": "each launch alone in plain stream order, between the library's CUDA "
+                                    "events on the launching stream",
+                     "in_stream": {"avg_launch_ms": stream_ms, "achieved": stream_achieved,
+                                   "frac": stream_achieved / hbm if stream_achieved else None,
+                                   "launch_mode": "the timed region's launches (layer calls back to back"
+                                                  + (" under programmatic dependent launch" if pdl else "")
+                                                  + "): timed region / launches"}},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
                 "layer_chunks": [len(ls) for ls in chunks], "outputs_equal_device_run": e2e_same},
@@ -767,6 +874,8 @@ def main():
     del cases
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_companions and args.workload == "pages_shape":
+        line["decode_workloads"] = decode_workloads(ekv, torch, peaks, min(args.steps, 20), args.warmup,
+                                                    args.seed)
         line["companions"] = companions(ekv, torch, peaks)
     if rank == 0:
         print(json.dumps(line))

@@ -323,19 +323,23 @@ ekv_status ekv_append_kv(ekv_ctx* ctx, const void* k_new, const void* v_new, voi
  * no counterpart of this call: it computes exactly what ekv_paged_decode computes, for
  * the shape given in its first three arguments, without a context.
  *
- * Its split-K scratch (partial records, tickets, flags) is one 16 MiB array of device
- * memory compiled into the library: every GPU that loads the library holds it until
- * the process exits. A call whose records need more than fits returns
- * EKV_ERR_CAPACITY ((batch + #SMs) * (8 / H_kv) * H_q * (D + 2) floats plus 256 KiB of
- * flags must fit in 16 MiB; batch <= 4096).
+ * Its split-K scratch (partial records, tickets, error word) is one 16 MiB array of
+ * device memory compiled into the library: every GPU that loads the library holds it
+ * until the process exits. The first 128 KiB hold the tickets (4,096 x 8 ints), then
+ * 256 B of error word, then the records, aligned to 256 B: (batch + #SMs) * (8 / H_kv)
+ * * H_q float2 (m, l) pairs and as many * D floats must fit in what is left; a call
+ * whose records need more returns EKV_ERR_CAPACITY (batch <= 4096).
  *  - The first call on a device looks up the array's device address (and the SM
  *    count) with that device current; make that first call before any stream capture.
- *  - Every call shares the one array and starts by clearing its flags on `stream`:
+ *    The address stays valid for the life of the device's primary context: do not use
+ *    this entry point on a device after cudaDeviceReset (the address looked up before
+ *    the reset would then be stale).
+ *  - Every call shares the one array and starts by clearing its tickets on `stream`:
  *    calls that overlap on the GPU (other streams, other host threads) race on it.
  *  - err_out: device int[4] that receives {ekv_status, ekv_detail, index, 0} of the
  *    first data error the kernel finds (zeroed by the call first), or NULL.
  * No cudaMalloc, cudaFree or allocating library call is made; work is enqueued on
- * `stream` (cudaMemsetAsync of the flags and err_out, then one kernel launch). The
+ * `stream` (cudaMemsetAsync of the tickets and err_out, then one kernel launch). The
  * other arguments and all layouts are those of ekv_paged_decode. */
 ekv_status ekv_paged_decode_noalloc(int num_q_heads, int num_kv_heads, int head_dim,
                                     const void* q, const void* k_pages, const void* v_pages,
@@ -346,9 +350,12 @@ ekv_status ekv_paged_decode_noalloc(int num_q_heads, int num_kv_heads, int head_
                                     const int32_t* seq_lens, int batch, float sm_scale,
                                     void* out, float* lse, int* err_out, void* stream);
 
-/* Synchronise the stream of the context's last call, read the sticky device error
- * word and clear it. *code is an ekv_status (EKV_OK or EKV_ERR_DEVICE_CHECK), *detail
- * an ekv_detail. Either pointer may be NULL. Returns EKV_ERR_CUDA if the sync fails. */
+/* Synchronise the stream of the context's last call (that stream only), read the
+ * sticky device error word and clear it; after an error the context's ticket buffer is
+ * cleared too, so a call that wound down early leaves nothing behind for the next one.
+ * *code is an ekv_status (EKV_OK or EKV_ERR_DEVICE_CHECK), *detail an ekv_detail. Either
+ * pointer may be NULL. Returns EKV_ERR_CUDA if the sync fails. After EKV_DETAIL_TIMEOUT
+ * the outputs of the call that reported it are undefined. */
 ekv_status ekv_get_error(ekv_ctx* ctx, int* code, int* detail);
 
 /* Kernel timing for measurement: when enabled, each ekv_paged_decode records CUDA
@@ -370,15 +377,24 @@ ekv_status ekv_set_decode_variant(ekv_ctx* ctx, int variant);
  * ekv_paged_decode_elastic (decode variant 0) are launched with programmatic stream
  * serialization and signal their own dependents at kernel start, so the next call's
  * prologue and first page fills run on SMs as this call's CTAs leave, overlapping its
- * merge tail. Ordering contract with the kernel immediately before the decode in the
- * stream: before its grid-dependency wait the decode reads seq_lens, the block tables,
- * page_mode, v_scales, boundaries and the K/V pages that are not the last page of
- * their sequence; it reads q and writes out, lse and its workspace only after the
- * preceding kernel has completed and its writes are visible. The preceding kernel may
- * therefore write q and the last page of each sequence (ekv_append_kv does exactly
- * that) but none of the other inputs. Kernels of this library never signal early
- * except the decode itself, which writes no decode input. With a preceding kernel
- * that does not signal (any other kernel, a copy, an event wait) nothing overlaps.
+ * merge tail.
+ * What CUDA guarantees, and therefore the contract: a kernel launched this way may
+ * start before the kernel ahead of it in the stream (the "primary") has finished, and
+ * the primary's memory writes are guaranteed visible to it only after its
+ * grid-dependency wait (CUDA C++ Programming Guide, "Programmatic Dependent Launch and
+ * Synchronization": cudaGridDependencySynchronize / griddepcontrol.wait). Before that
+ * wait the decode reads seq_lens, the block tables, page_mode, v_scales, boundaries and
+ * the K/V pages that are not the last page of their sequence; it reads q and writes
+ * out, lse and its workspace only after the wait. So the kernel immediately ahead of
+ * the decode in the stream may write q and the last page of each sequence
+ * (ekv_append_kv does exactly that) but none of the other inputs.
+ * The library keeps that rule for its own kernels: the page-mode transitions
+ * (ekv_demote_pages, ekv_demote_pages_base, ekv_promote_pages, ekv_transition_pages)
+ * write value pages, mode bytes and scales, so a decode enqueued on a stream whose last
+ * kernel from this library (any context) is a transition is launched in plain stream
+ * order, with no overlap; the decode, gather, prefill and writer write no input that the
+ * decode reads before its wait. For kernels of other code the caller keeps the rule
+ * (e.g. with an event wait or a library call in between, which ends the overlap).
  * enable = 0 (default): ordinary stream order. Returns EKV_ERR_INVALID_ARG for a
  * null context or another value. */
 ekv_status ekv_set_pdl(ekv_ctx* ctx, int enable);

@@ -2,6 +2,11 @@
 
 No CMake: each translation unit is compiled in parallel, then linked with the static
 CUDA runtime. The result is written atomically next to this file.
+
+A second library, libekv_waittest.so, is built beside it for the tests only: the
+decode translation units compiled with EKV_TEST_WAIT_TIMEOUT (a 5 ms bound on the
+pipeline waits and an entry point that makes one wait run out), linked with the other
+objects of the production build. Nothing but the tests loads it.
 """
 
 import concurrent.futures
@@ -17,7 +22,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libekv.so")
+TEST_LIB = os.path.join(HERE, "libekv_waittest.so")
 SOURCES = ["ekv_api.cu", "decode_simt.cu", "decode_mma.cu", "gather_demote.cu", "noalloc.cu", "prefill_mma.cu", "prefill_tc05.cu"]
+# translation units that see DecodeParams or the wait bound: rebuilt for the test library
+TEST_SOURCES = ["ekv_api.cu", "decode_simt.cu", "decode_mma.cu", "noalloc.cu"]
+TEST_DEFINE = "-DEKV_TEST_WAIT_TIMEOUT"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "--expt-relaxed-constexpr", "-I", INCLUDE]
@@ -36,42 +45,54 @@ def _inputs():
 
 
 def up_to_date():
-    if not os.path.exists(LIB):
-        return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(f) <= t for f in _inputs())
+    for lib in (LIB, TEST_LIB):
+        if not os.path.exists(lib):
+            return False
+        t = os.path.getmtime(lib)
+        if not all(os.path.getmtime(f) <= t for f in _inputs()):
+            return False
+    return True
+
+
+def _link(cc, objs, lib):
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=HERE)
+    os.close(fd)
+    cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        os.unlink(tmp)
+        raise RuntimeError(f"link failed:\n{r.stderr}")
+    os.replace(tmp, lib)
 
 
 def build(force=False, verbose=False, ptxas_info=False):
-    """Compile and link libekv.so; returns its path."""
+    """Compile and link libekv.so and the tests' libekv_waittest.so; returns libekv.so's path."""
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [cc] + FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        src, test = job
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", "_waittest.o" if test else ".o"))
+        cmd = [cc] + FLAGS + extra + ([TEST_DEFINE] if test else []) + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed for {src}{' (test build)' if test else ''}:\n{r.stderr}")
         return obj, r.stderr
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    jobs = [(s, False) for s in SOURCES] + [(s, True) for s in TEST_SOURCES]
+    # the largest translation units first, so the pool is not left waiting on one of them
+    jobs.sort(key=lambda j: -os.path.getsize(os.path.join(CSRC, j[0])))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+        results = dict(zip(jobs, ex.map(compile_one, jobs)))
     if verbose or ptxas_info:
-        for _, log in results:
-            if log:
+        for (src, test), (_, log) in results.items():
+            if log and not test:
                 sys.stderr.write(log)
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=HERE)
-    os.close(fd)
-    cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        os.unlink(tmp)
-        raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    _link(cc, [results[(s, False)][0] for s in SOURCES], LIB)
+    _link(cc, [results[(s, s in TEST_SOURCES)][0] for s in SOURCES], TEST_LIB)
     return LIB
 
 

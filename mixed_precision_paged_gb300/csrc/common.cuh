@@ -16,7 +16,12 @@ namespace ekv {
 constexpr int kPage = 16;                 // tokens per page (page size 16)
 constexpr int kMaxKvHeads = 8;
 constexpr int kMaxBatch = 4096;
+#ifdef EKV_TEST_WAIT_TIMEOUT
+// Test build only (libekv_waittest.so): a short bound, so a test can run a wait out
+constexpr uint64_t kWaitTimeoutNs = 5000000ull;      // 5 ms
+#else
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;   // 1 s bound on every pipeline wait
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -66,6 +71,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+
+#ifdef EKV_TEST_WAIT_TIMEOUT
+// Test build only: raise the byte count the barrier's current phase waits for, without
+// arriving. Bytes that no copy delivers keep the phase open, so the wait on it runs out
+// while no copy is left in flight.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+#endif
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");

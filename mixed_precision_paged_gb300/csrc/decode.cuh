@@ -62,6 +62,10 @@ struct DecodeParams {
   // and the K/V pages that are not the last page of their sequence; q is read and every
   // output, record and ticket written after it.
   int pdl;
+#ifdef EKV_TEST_WAIT_TIMEOUT
+  // test build only: 1 makes the first ring wait of CTA 0, warp 0 run out
+  int inject_timeout;
+#endif
 };
 
 constexpr int kMetaCompact = 1;   // E4M3 value page

@@ -121,6 +121,10 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
   // nxt = next batch (mode bytes / scales in flight), nxt2 = the one after (ids in flight)
   const float tensor_scale =
       (VMODE != kVFP16 && p.scale_mode == EKV_SCALE_PER_TENSOR && p.v_scales) ? __ldg(p.v_scales) : 0.f;
+#ifdef EKV_TEST_WAIT_TIMEOUT
+  // test build only: 16 bytes more than any copy delivers on slot 0's first phase
+  if (p.inject_timeout && blockIdx.x == 0 && warp == 0 && lane == 0 && n_my > 0) mbar_expect_tx(&ring.full[0], 16);
+#endif
   WarpMeta cur, nxt, nxt2;
   wm_ids<EL>(p, cu, start, n_my, lane, cur);
   wm_ids<EL>(p, cu, start, n_my, 32 + lane, nxt);

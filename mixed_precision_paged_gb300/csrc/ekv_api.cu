@@ -6,6 +6,7 @@
 
 #include <mutex>
 #include <new>
+#include <unordered_set>
 #include <vector>
 
 #include "decode.cuh"
@@ -56,6 +57,31 @@ struct DeviceGuard {
     if (prev >= 0) cudaSetDevice(prev);
   }
 };
+
+// Streams whose last kernel enqueued by this library (from any context) writes what a
+// decode reads before its grid-dependency wait: the page-mode transitions write value
+// pages, mode bytes and scales. CUDA makes a preceding grid's writes visible to a
+// programmatically launched kernel only after that kernel's griddepcontrol.wait, so the
+// next decode on such a stream is launched without programmatic serialization. Every
+// other launch of the library removes its stream from the set.
+std::mutex g_writer_mu;
+std::unordered_set<cudaStream_t> g_writer_streams;
+
+void note_launch(cudaStream_t st, bool writes_decode_inputs) {
+  std::lock_guard<std::mutex> lock(g_writer_mu);
+  if (writes_decode_inputs) g_writer_streams.insert(st);
+  else g_writer_streams.erase(st);
+}
+
+bool follows_writer(cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_writer_mu);
+  return g_writer_streams.count(st) != 0;
+}
+
+#ifdef EKV_TEST_WAIT_TIMEOUT
+// test build only: decode calls left that run their first ring wait out
+int g_inject_timeout_calls = 0;
+#endif
 
 bool supported_shape(int Hq, int Hkv, int D) {
   if (D != 64 && D != 128) return false;
@@ -207,9 +233,16 @@ ekv_status decode_impl(ekv_ctx* c, const void* q, const void* k_pages, const voi
   p.num_v_slots = elastic ? num_v_slots : num_pages;
   p.elastic = elastic ? 1 : 0;
   p.pdl = c->pdl && c->variant == 0 ? 1 : 0;
+#ifdef EKV_TEST_WAIT_TIMEOUT
+  if (g_inject_timeout_calls > 0 && c->variant == 0) {
+    p.inject_timeout = 1;
+    --g_inject_timeout_calls;
+  }
+#endif
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   c->last_stream = st;
+  if (p.pdl && follows_writer(st)) p.pdl = 0;      // right after a transition: plain stream order
   const bool timed = c->profiling && c->ev_used * 2 + 1 < c->ev.size();
   if (timed) cudaEventRecord(c->ev[2 * c->ev_used], st);
   const int algo = c->variant == 1 ? kAlgoSimt : kAlgoMma;
@@ -217,6 +250,7 @@ ekv_status decode_impl(ekv_ctx* c, const void* q, const void* k_pages, const voi
   cudaError_t e = algo == kAlgoSimt ? launch_split_simt(tk, t8, t16, p, D, vmode, c->split_ctas, smem, st)
                                     : launch_split_mma(tk, t8, t16, p, D, vmode, c->split_ctas, smem, st);
   if (e != cudaSuccess) return EKV_ERR_CUDA;
+  note_launch(st, false);
   if (timed) {
     cudaEventRecord(c->ev[2 * c->ev_used + 1], st);
     ++c->ev_used;
@@ -330,6 +364,7 @@ ekv_status gather_impl(ekv_ctx* c, const void* k_pages, const void* v_pages, lon
     if (launch_gather(p, r, off, st) != cudaSuccess) return EKV_ERR_CUDA;
     base += off;
   }
+  note_launch(st, false);
   return EKV_OK;
 }
 
@@ -395,7 +430,9 @@ ekv_status transition(ekv_ctx* c, int op, void* v_pages, long long v_page_stride
   p.Hkv = Hkv;
   p.D = D;
   p.err = c->err;
-  return launch_transition(p, op, n, c->num_sms, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+  if (launch_transition(p, op, n, c->num_sms, st) != cudaSuccess) return EKV_ERR_CUDA;
+  note_launch(st, true);
+  return EKV_OK;
 }
 
 }  // namespace
@@ -467,7 +504,9 @@ ekv_status ekv_append_kv(ekv_ctx* c, const void* k_new, const void* v_new, void*
   p.Hkv = Hkv;
   p.D = D;
   p.err = c->err;
-  return launch_append(p, batch, st) == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+  if (launch_append(p, batch, st) != cudaSuccess) return EKV_ERR_CUDA;
+  note_launch(st, false);
+  return EKV_OK;
 }
 
 ekv_status ekv_prefill_attention(ekv_ctx* c, const void* q, const void* ws_k, const void* ws_v, int ws_pages,
@@ -501,20 +540,26 @@ ekv_status ekv_prefill_attention(ekv_ctx* c, const void* q, const void* ws_k, co
   p.qscale = sm_scale * 1.4426950408889634f;
   p.err = c->err;
   const cudaError_t e = c->variant == 1 ? launch_prefill(p, D, max_len, st) : launch_prefill_tc05(p, D, max_len, st);
-  return e == cudaSuccess ? EKV_OK : EKV_ERR_CUDA;
+  if (e != cudaSuccess) return EKV_ERR_CUDA;
+  note_launch(st, false);
+  return EKV_OK;
 }
 
 ekv_status ekv_get_error(ekv_ctx* c, int* code, int* detail) {
   if (!c) return EKV_ERR_INVALID_ARG;
   DeviceGuard g(c->device);
-  if (cudaStreamSynchronize(c->last_stream) != cudaSuccess) return EKV_ERR_CUDA;
+  cudaStream_t st = c->last_stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return EKV_ERR_CUDA;
   int h[4] = {0, 0, 0, 0};
-  if (cudaMemcpy(h, c->err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return EKV_ERR_CUDA;
-  if (cudaMemset(c->err, 0, sizeof(h)) != cudaSuccess) return EKV_ERR_CUDA;
+  if (cudaMemcpyAsync(h, c->err, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(c->err, 0, sizeof(h), st) != cudaSuccess)
+    return EKV_ERR_CUDA;
   // after a device error (a kernel may have wound down early) start the next call from
-  // a clean plan buffer: no stale tickets
-  if (h[0] != 0 && cudaMemset(c->plan, 0, kPlanInts * sizeof(int)) != cudaSuccess) return EKV_ERR_CUDA;
-  if (cudaDeviceSynchronize() != cudaSuccess) return EKV_ERR_CUDA;
+  // a clean plan buffer: no stale tickets. Only the context's stream is synchronised.
+  if (cudaStreamSynchronize(st) != cudaSuccess) return EKV_ERR_CUDA;
+  if (h[0] != 0 && (cudaMemsetAsync(c->plan, 0, kPlanInts * sizeof(int), st) != cudaSuccess ||
+                    cudaStreamSynchronize(st) != cudaSuccess))
+    return EKV_ERR_CUDA;
   if (code) *code = h[0];
   if (detail) *detail = h[1];
   return EKV_OK;
@@ -547,6 +592,17 @@ ekv_status ekv_profile_read(ekv_ctx* c, double* split_ms, long long* launches) {
   c->ev_used = 0;
   return EKV_OK;
 }
+
+#ifdef EKV_TEST_WAIT_TIMEOUT
+// Test build only (libekv_waittest.so; not declared in ekv.h): the next `calls` decode
+// calls (tensor-core consumer) make the first ring wait of CTA 0, warp 0 run out, so a
+// test can check the timeout report and that the context is usable afterwards.
+ekv_status ekv_test_inject_wait_timeout(int calls) {
+  if (calls < 0) return EKV_ERR_INVALID_ARG;
+  g_inject_timeout_calls = calls;
+  return EKV_OK;
+}
+#endif
 
 ekv_status ekv_query(ekv_ctx* c, int* num_sms, int* split_ctas) {
   if (!c) return EKV_ERR_INVALID_ARG;

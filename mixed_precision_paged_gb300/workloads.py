@@ -228,6 +228,47 @@ def gather_demote_shape():
 
 # ------------------------------------------------------------ device-side generation
 
+@dataclass
+class GatherDemoteCase:
+    """Device tensors of the gather/demotion workload (32 prompts x 8192 tokens)."""
+    k_pages: object           # fp16 [P][16][H_kv][D]
+    v8_pages: object          # uint8 [P][16*H_kv*D] E4M3 codes (uniform compact pool)
+    v_scales: object          # fp32 [P][H_kv] per-(page, KV head) scales
+    block_table: object       # int32 [prompts][pages per prompt], a permutation of the pool
+    chunks: list              # host int32 [n][3] page ranges {seq, first, num}, one per chunk
+    ws_pages: int
+    v16_pages: object         # uint8 [P][16*H_kv*D*2]: the FP16 pool given to demotion
+    demote_ids: object        # int32 [P * fraction] distinct page ids to demote
+
+
+def device_gather_demote_case(seed=1004, device="cuda", prompts=32, tokens=8192, num_kv_heads=8,
+                              head_dim=128, ws_pages=4096, chunk_prompts=8, demote_fraction=0.5,
+                              demote_std=math.sqrt(2.0)):
+    """The gather/demotion workload on the device: K ~ N(0, 1) fp16; V ~ N(0, 1) stored as
+    E4M3 codes with absmax/448 scales per (page, KV head); prompts' pages at a random
+    permutation of the pool; gather ranges of ``chunk_prompts`` whole prompts per chunk;
+    a separate FP16 value pool ~ N(0, demote_std^2) and a random ``demote_fraction`` of
+    its page ids for demotion."""
+    S, H, D = PAGE_SIZE, num_kv_heads, head_dim
+    per = (tokens + S - 1) // S
+    P = prompts * per
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    k = torch.randn((P, S, H, D), generator=g, device=device).to(torch.float16)
+    vv = torch.randn((P, S, H, D), generator=g, device=device)
+    a = vv.abs().amax(dim=(1, 3))
+    sc = torch.where(a > 0, a / 448.0, torch.ones_like(a)).contiguous()
+    v8 = _e4m3_codes(vv / sc[:, None, :, None]).reshape(P, -1)
+    del vv
+    bt = torch.randperm(P, generator=g, device=device).to(torch.int32).reshape(prompts, per)
+    chunks = [np.array([[s, 0, per] for s in range(c, min(prompts, c + chunk_prompts))], dtype=np.int32)
+              for c in range(0, prompts, chunk_prompts)]
+    v16 = (torch.randn((P, S, H, D), generator=g, device=device) * demote_std).to(torch.float16)
+    ids = torch.randperm(P, generator=g, device=device)[: int(P * demote_fraction)].to(torch.int32)
+    return GatherDemoteCase(k_pages=k, v8_pages=v8, v_scales=sc, block_table=bt, chunks=chunks,
+                            ws_pages=ws_pages, v16_pages=v16.view(torch.uint8).reshape(P, -1), demote_ids=ids)
+
+
 def device_decode_case(seq_lens, num_q_heads, num_kv_heads, head_dim, *, v_format="e4m3",
                        scale_mode=SCALE_PER_TENSOR, seed=0, device="cuda", p_compact=0.5,
                        pool_slack=0, poison_tail=True, p_base=0.0):

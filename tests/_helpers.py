@@ -60,3 +60,46 @@ def assert_close(out_gpu, lse_gpu, out_ref, lse_ref, rows=None):
             le = np.abs(l[fin] - lse_ref[fin]).max()
             assert le <= LSE_ATOL, f"lse error {le:.3e} > {LSE_ATOL}"
     return float(err.max())
+
+
+# -------------------------------------------------------- the oracle over many sequences
+
+def sequence_subcases(d, idx):
+    """One host case per sequence of device case ``d`` in ``idx``, each holding only the
+    pages that sequence reads, in a compact pool with its block table renumbered (the
+    oracle then reads the same data as the kernel did)."""
+    import torch
+    bt = d.block_table.cpu().numpy()
+    sl = d.seq_lens.cpu().numpy()
+    per_page_scales = d.v_scales is not None and d.v_scales.dim() == 2
+    q = d.q.cpu().numpy()
+    out = []
+    for b in idx:
+        n = (int(sl[b]) + 15) // 16
+        pages = bt[b, :n].astype(np.int64)
+        pid = torch.from_numpy(pages).to(d.k_pages.device)
+        out.append(wl.DecodeCase(
+            q=q[b:b + 1], k_pages=d.k_pages[pid].cpu().numpy(), v_pages=d.v_pages[pid].cpu().numpy(),
+            v_scales=None if d.v_scales is None else
+            (d.v_scales[pid] if per_page_scales else d.v_scales).cpu().numpy(),
+            scale_mode=d.scale_mode, page_mode=None if d.page_mode is None else d.page_mode[pid].cpu().numpy(),
+            uniform_mode=d.uniform_mode, block_table=np.arange(max(n, 1), dtype=np.int32)[None, :],
+            seq_lens=sl[b:b + 1].astype(np.int32), num_q_heads=d.num_q_heads,
+            num_kv_heads=d.num_kv_heads, head_dim=d.head_dim))
+    return out
+
+
+def _oracle_one(case):
+    out, lse = oracle_decode(case)
+    return out[0], lse[0]
+
+
+def oracle_decode_sequences(subcases):
+    """The float64 oracle over single-sequence cases, one single-threaded spawn worker per
+    host core (a pool started by spawn is safe after CUDA has been initialised)."""
+    import multiprocessing as mp
+    import os
+    n = max(1, min(len(subcases), os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_oracle_one, subcases, chunksize=1)
+    return np.stack([r[0] for r in res]), np.stack([r[1] for r in res])

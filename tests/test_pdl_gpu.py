@@ -156,3 +156,147 @@ def test_switch_values_and_the_cuda_core_consumer(ekv_lib, torch_cuda):
     ro, rl = oracle_decode(case)
     assert_close(out, lse, ro, rl)
 
+
+
+def _decode_into(ekv_lib, ctx, case, d, v, mode, scales, out, lse, stream):
+    ekv_lib.ekv_paged_decode(ctx.handle, d.q, d.k_pages, v, case.v_page_stride, case.num_pages, scales,
+                             case.scale_mode, mode, case.uniform_mode, d.block_table,
+                             case.block_table.shape[1], d.seq_lens, case.batch, 0.0, out, lse, stream)
+
+
+def _reps_match(outs, lses, ref):
+    ro, rl = ref
+    for o, l in zip(outs, lses):
+        assert_close(o, l, ro, rl)
+
+
+def test_decode_right_after_each_transition(ekv_lib, torch_cuda):
+    """ElasticKV's step order (Sec. 3.4, "Transition protocols": a page's new state is
+    visible only after its transition completes): a transition of the library, then at
+    once, in the same stream, a decode with the programmatic launch switched on that
+    reads the pages just transitioned, non-last pages included. The transitions run on a
+    second context, so the rule that ends the overlap after them holds across contexts.
+    Each step order is repeated a few hundred times; every decode must match the oracle
+    on the post-transition state."""
+    torch = torch_cuda
+    from oracle import base as ob
+    from oracle import demote as odm
+    lens = [700, 33, 1500, 16, 250, 1]
+    hq, hkv, d = 32, 8, 128
+    case = wl.make_decode_case(lens, hq, hkv, d, v_format="mixed", scale_mode=1, seed=910, poison=False,
+                               pool_pages=sum((x + 15) // 16 for x in lens) + 4, p_compact=0.3, p_base=0.2)
+    B, P, n = case.batch, case.num_pages, 16 * hkv * d
+    used = sorted({int(case.block_table[b, j]) for b in range(B) for j in range((lens[b] + 15) // 16)})
+    ids_np = np.array([p for p in used if case.page_mode[p] == 0], np.int32)
+    last = {int(case.block_table[b, (lens[b] - 1) // 16]) for b in range(B)}
+    assert any(p not in last for p in ids_np)          # non-last pages are transitioned
+    dv = to_device(case)
+    dec = ekv_lib.Context(hq, hkv, d, B, pdl=True)
+    trans = ekv_lib.Context(hq, hkv, d, B)
+    st = torch.cuda.current_stream()
+    ids = torch.from_numpy(ids_np).cuda()
+    v0, m0, s0 = dv.v_pages.clone(), dv.page_mode.clone(), dv.v_scales.clone()
+    v, mode, sc = v0.clone(), m0.clone(), s0.clone()
+    reps = 200
+
+    def new_outs():
+        return ([torch.empty((B, hq, d), dtype=torch.float16, device="cuda") for _ in range(reps)],
+                [torch.empty((B, hq), dtype=torch.float32, device="cuda") for _ in range(reps)])
+
+    def oracle_state(vv, mm, ss):
+        c = wl.DecodeCase(**{**case.__dict__})
+        c.v_pages, c.page_mode, c.v_scales = vv, mm, ss
+        return oracle_decode(c)
+
+    # E4M3 demotion, then decode (pages reset by copies before each demotion)
+    outs, lses = new_outs()
+    for r in range(reps):
+        v.copy_(v0)
+        mode.copy_(m0)
+        sc.copy_(s0)
+        ekv_lib.ekv_demote_pages(trans.handle, v, case.v_page_stride, P, ids, len(ids_np), mode, sc, st)
+        _decode_into(ekv_lib, dec, case, dv, v, mode, sc, outs[r], lses[r], st)
+    torch.cuda.synchronize()
+    assert dec.error() == (0, 0) and trans.error() == (0, 0)
+    rv, rm, rs = odm.demote_pages(case.v_pages, ids_np, case.page_mode, case.v_scales, hkv, d)
+    assert np.array_equal(mode.cpu().numpy(), rm) and np.array_equal(v.cpu().numpy(), rv)
+    _reps_match(outs, lses, oracle_state(rv, rm, rs))
+
+    # BASE demotion then decode, promotion then decode, alternating on the same pages
+    v.copy_(v0)
+    mode.copy_(m0)
+    low = torch.empty((len(ids_np), n), dtype=torch.uint8, device="cuda")
+    outs_b, lses_b = new_outs()
+    outs_p, lses_p = new_outs()
+    for r in range(reps):
+        ekv_lib.ekv_demote_pages_base(trans.handle, v, case.v_page_stride, P, ids, len(ids_np), mode, low, st)
+        _decode_into(ekv_lib, dec, case, dv, v, mode, s0, outs_b[r], lses_b[r], st)
+        ekv_lib.ekv_promote_pages(trans.handle, v, case.v_page_stride, P, ids, len(ids_np), mode, low, st)
+        _decode_into(ekv_lib, dec, case, dv, v, mode, s0, outs_p[r], lses_p[r], st)
+    torch.cuda.synchronize()
+    assert dec.error() == (0, 0) and trans.error() == (0, 0)
+    bv, bm, _, _ = ob.demote_to_base(case.v_pages, ids_np, case.page_mode, hkv, d)
+    assert torch.equal(v, v0)                          # exact round trips
+    _reps_match(outs_b, lses_b, oracle_state(bv, bm, case.v_scales))
+    _reps_match(outs_p, lses_p, oracle_state(case.v_pages, case.page_mode, case.v_scales))
+    dec.close()
+    trans.close()
+
+
+def test_elastic_decode_right_after_pair_packing(ekv_lib, torch_cuda):
+    """The pair-structured layout: two located transitions pack pairs (A, B) of TARGET
+    pages into A's slot (A in place, then B into half 1 of A's slot), and the elastic
+    decode, launched at once with the programmatic switch on, reads the packed values
+    through the value block table written before the transitions. Repeated a few
+    hundred times from the same start; every decode must match the oracle."""
+    torch = torch_cuda
+    from oracle import elastic as oe
+    lens = [16 * 30, 16 * 21 + 5, 37, 16 * 12]
+    hq, hkv, d = 32, 8, 128
+    case = wl.make_decode_case(lens, hq, hkv, d, v_format="fp16", seed=920, poison=False,
+                               pool_pages=sum((x + 15) // 16 for x in lens) + 2)
+    B, P = case.batch, case.num_pages
+    bt = case.block_table
+    pairs = [(int(bt[b, j]), int(bt[b, j + 1])) for b in (0, 1, 3) for j in range(0, 10, 2)]
+    a_np = np.array([x for x, _ in pairs], np.int32)
+    b_np = np.array([y for _, y in pairs], np.int32)
+    vtab = 2 * bt.copy()
+    for x, y in pairs:
+        vtab[bt == y] = 2 * x + 1
+    r1 = oe.transition(oe.OP_TO_E4M3, case.v_pages, a_np, None, None, np.zeros(P, np.uint8),
+                       np.ones((P, hkv), np.float32), None, hkv, d)
+    r2 = oe.transition(oe.OP_TO_E4M3, r1[0], b_np, 2 * b_np, 2 * a_np + 1, r1[1], r1[2], None, hkv, d)
+    ref = oe.paged_decode_elastic(case.q, case.k_pages, r2[0], r2[2], 1, r2[1], 0, bt, vtab, None, 1,
+                                  case.seq_lens)
+    dv = to_device(case)
+    dec = ekv_lib.Context(hq, hkv, d, B, pdl=True)
+    trans = ekv_lib.Context(hq, hkv, d, B)
+    st = torch.cuda.current_stream()
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()   # noqa: E731
+    v0, vtab0, vtab_d = dv.v_pages.clone(), t(2 * bt), t(vtab)
+    a, b, srcb, dstb = t(a_np), t(b_np), t(2 * b_np), t(2 * a_np + 1)
+    v = v0.clone()
+    mode = torch.zeros(P, dtype=torch.uint8, device="cuda")
+    sc = torch.ones((P, hkv), dtype=torch.float32, device="cuda")
+    vt = vtab0.clone()
+    reps = 200
+    outs = [torch.empty((B, hq, d), dtype=torch.float16, device="cuda") for _ in range(reps)]
+    lses = [torch.empty((B, hq), dtype=torch.float32, device="cuda") for _ in range(reps)]
+    for r in range(reps):
+        v.copy_(v0)
+        mode.zero_()
+        sc.fill_(1.0)
+        vt.copy_(vtab_d)                                 # the caller's value table, before the transitions
+        ekv_lib.ekv_transition_pages(trans.handle, oe.OP_TO_E4M3, v, case.v_page_stride, P, P, a, None, None,
+                                     len(a_np), mode, sc, None, st)
+        ekv_lib.ekv_transition_pages(trans.handle, oe.OP_TO_E4M3, v, case.v_page_stride, P, P, b, srcb, dstb,
+                                     len(b_np), mode, sc, None, st)
+        ekv_lib.ekv_paged_decode_elastic(dec.handle, dv.q, dv.k_pages, v, case.v_page_stride, P, P, sc, 1, mode,
+                                         0, dv.block_table, vt, bt.shape[1], None, 1, dv.seq_lens, B, 0.0,
+                                         outs[r], lses[r], st)
+    torch.cuda.synchronize()
+    assert dec.error() == (0, 0) and trans.error() == (0, 0)
+    assert np.array_equal(v.cpu().numpy(), r2[0]) and np.array_equal(mode.cpu().numpy(), r2[1])
+    _reps_match(outs, lses, ref)
+    dec.close()
+    trans.close()
