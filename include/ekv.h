@@ -372,29 +372,34 @@ ekv_status ekv_profile_read(ekv_ctx* ctx, double* split_ms, long long* launches)
  * compute the same function; 1 exists for measurement. */
 ekv_status ekv_set_decode_variant(ekv_ctx* ctx, int variant);
 
-/* Programmatic dependent launch of the decode (CUDA's griddepcontrol, sm_90+), for
- * a stream of back-to-back calls (one per layer). enable = 1: ekv_paged_decode and
- * ekv_paged_decode_elastic (decode variant 0) are launched with programmatic stream
- * serialization and signal their own dependents at kernel start, so the next call's
- * prologue and first page fills run on SMs as this call's CTAs leave, overlapping its
- * merge tail.
+/* Programmatic dependent launch (CUDA's griddepcontrol, sm_90+) of the decode and the
+ * gather, for streams of back-to-back calls (a decode per layer; the gather chunks of a
+ * prefill admission). enable = 1: ekv_paged_decode, ekv_paged_decode_elastic (decode
+ * variant 0), ekv_gather_prefill and ekv_gather_prefill_elastic are launched with
+ * programmatic stream serialization and signal their own dependents at kernel start,
+ * so the next call's first reads run on SMs as this call's CTAs leave.
  * What CUDA guarantees, and therefore the contract: a kernel launched this way may
  * start before the kernel ahead of it in the stream (the "primary") has finished, and
  * the primary's memory writes are guaranteed visible to it only after its
  * grid-dependency wait (CUDA C++ Programming Guide, "Programmatic Dependent Launch and
- * Synchronization": cudaGridDependencySynchronize / griddepcontrol.wait). Before that
- * wait the decode reads seq_lens, the block tables, page_mode, v_scales, boundaries and
- * the K/V pages that are not the last page of their sequence; it reads q and writes
- * out, lse and its workspace only after the wait. So the kernel immediately ahead of
- * the decode in the stream may write q and the last page of each sequence
- * (ekv_append_kv does exactly that) but none of the other inputs.
- * The library keeps that rule for its own kernels: the page-mode transitions
+ * Synchronization": cudaGridDependencySynchronize / griddepcontrol.wait).
+ *  - Before that wait the decode reads seq_lens, the block tables, page_mode, v_scales,
+ *    boundaries and the K/V pages that are not the last page of their sequence; it
+ *    reads q and writes out, lse and its workspace after the wait. The kernel
+ *    immediately ahead of a decode may therefore write q and the last page of each
+ *    sequence (ekv_append_kv does exactly that) but none of the other inputs.
+ *  - Before that wait the gather reads the block tables, page_mode, v_scales,
+ *    boundaries and every K/V page it copies; it writes the workspace, the indices and
+ *    the error word after the wait. The kernel immediately ahead of a gather may write
+ *    none of its inputs.
+ * The library keeps these rules for its own kernels: the page-mode transitions
  * (ekv_demote_pages, ekv_demote_pages_base, ekv_promote_pages, ekv_transition_pages)
- * write value pages, mode bytes and scales, so a decode enqueued on a stream whose last
- * kernel from this library (any context) is a transition is launched in plain stream
- * order, with no overlap; the decode, gather, prefill and writer write no input that the
- * decode reads before its wait. For kernels of other code the caller keeps the rule
- * (e.g. with an event wait or a library call in between, which ends the overlap).
+ * write value pages, mode bytes and scales, and ekv_append_kv writes pool pages, so a
+ * decode enqueued on a stream whose last kernel from this library (any context) is a
+ * transition, and a gather whose last such kernel is a transition or the writer, is
+ * launched in plain stream order, with no overlap. The decode, gather and prefill write
+ * none of these inputs. For kernels of other code the caller keeps the rules (an event
+ * wait or a call of this library in between also ends the overlap).
  * enable = 0 (default): ordinary stream order. Returns EKV_ERR_INVALID_ARG for a
  * null context or another value. */
 ekv_status ekv_set_pdl(ekv_ctx* ctx, int enable);

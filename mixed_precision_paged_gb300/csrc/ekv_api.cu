@@ -6,7 +6,7 @@
 
 #include <mutex>
 #include <new>
-#include <unordered_set>
+#include <unordered_map>
 #include <vector>
 
 #include "decode.cuh"
@@ -58,24 +58,28 @@ struct DeviceGuard {
   }
 };
 
-// Streams whose last kernel enqueued by this library (from any context) writes what a
-// decode reads before its grid-dependency wait: the page-mode transitions write value
-// pages, mode bytes and scales. CUDA makes a preceding grid's writes visible to a
-// programmatically launched kernel only after that kernel's griddepcontrol.wait, so the
-// next decode on such a stream is launched without programmatic serialization. Every
-// other launch of the library removes its stream from the set.
-std::mutex g_writer_mu;
-std::unordered_set<cudaStream_t> g_writer_streams;
+// The kind of the last kernel this library (any context) enqueued on each stream, kept
+// for the streams where it writes what a programmatically launched kernel of the
+// library reads before its griddepcontrol.wait: the page-mode transitions write value
+// pages, mode bytes and scales; the cache writer writes the last page of each sequence.
+// CUDA makes a preceding grid's writes visible to a programmatically launched kernel
+// only after that kernel's wait, so a decode after a transition, and a gather after a
+// transition or the writer, is launched in plain stream order. Other launches (decode,
+// gather, prefill) remove their stream from the map.
+enum LastKernel { kAfterReader = 0, kAfterAppend = 1, kAfterTransition = 2 };
+std::mutex g_last_mu;
+std::unordered_map<cudaStream_t, int> g_last_kernel;
 
-void note_launch(cudaStream_t st, bool writes_decode_inputs) {
-  std::lock_guard<std::mutex> lock(g_writer_mu);
-  if (writes_decode_inputs) g_writer_streams.insert(st);
-  else g_writer_streams.erase(st);
+void note_launch(cudaStream_t st, int kind) {
+  std::lock_guard<std::mutex> lock(g_last_mu);
+  if (kind != kAfterReader) g_last_kernel[st] = kind;
+  else g_last_kernel.erase(st);
 }
 
-bool follows_writer(cudaStream_t st) {
-  std::lock_guard<std::mutex> lock(g_writer_mu);
-  return g_writer_streams.count(st) != 0;
+int last_kernel(cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_last_mu);
+  auto it = g_last_kernel.find(st);
+  return it == g_last_kernel.end() ? kAfterReader : it->second;
 }
 
 #ifdef EKV_TEST_WAIT_TIMEOUT
@@ -242,7 +246,7 @@ ekv_status decode_impl(ekv_ctx* c, const void* q, const void* k_pages, const voi
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   c->last_stream = st;
-  if (p.pdl && follows_writer(st)) p.pdl = 0;      // right after a transition: plain stream order
+  if (p.pdl && last_kernel(st) == kAfterTransition) p.pdl = 0;   // plain stream order after a transition
   const bool timed = c->profiling && c->ev_used * 2 + 1 < c->ev.size();
   if (timed) cudaEventRecord(c->ev[2 * c->ev_used], st);
   const int algo = c->variant == 1 ? kAlgoSimt : kAlgoMma;
@@ -250,7 +254,7 @@ ekv_status decode_impl(ekv_ctx* c, const void* q, const void* k_pages, const voi
   cudaError_t e = algo == kAlgoSimt ? launch_split_simt(tk, t8, t16, p, D, vmode, c->split_ctas, smem, st)
                                     : launch_split_mma(tk, t8, t16, p, D, vmode, c->split_ctas, smem, st);
   if (e != cudaSuccess) return EKV_ERR_CUDA;
-  note_launch(st, false);
+  note_launch(st, kAfterReader);
   if (timed) {
     cudaEventRecord(c->ev[2 * c->ev_used + 1], st);
     ++c->ev_used;
@@ -347,6 +351,7 @@ ekv_status gather_impl(ekv_ctx* c, const void* k_pages, const void* v_pages, lon
   p.num_v_slots = num_v_slots;
   p.boundaries = v_block_table ? boundaries : nullptr;
   p.has_base = v_block_table ? has_base : 1;
+  p.pdl = c->pdl && last_kernel(st) == kAfterReader ? 1 : 0;   // not right after a writer of the pool
   int base = 0;
   for (int i0 = 0; i0 < n; i0 += kMaxRanges) {
     GatherRanges r;
@@ -364,7 +369,7 @@ ekv_status gather_impl(ekv_ctx* c, const void* k_pages, const void* v_pages, lon
     if (launch_gather(p, r, off, st) != cudaSuccess) return EKV_ERR_CUDA;
     base += off;
   }
-  note_launch(st, false);
+  note_launch(st, kAfterReader);
   return EKV_OK;
 }
 
@@ -431,7 +436,7 @@ ekv_status transition(ekv_ctx* c, int op, void* v_pages, long long v_page_stride
   p.D = D;
   p.err = c->err;
   if (launch_transition(p, op, n, c->num_sms, st) != cudaSuccess) return EKV_ERR_CUDA;
-  note_launch(st, true);
+  note_launch(st, kAfterTransition);
   return EKV_OK;
 }
 
@@ -505,7 +510,7 @@ ekv_status ekv_append_kv(ekv_ctx* c, const void* k_new, const void* v_new, void*
   p.D = D;
   p.err = c->err;
   if (launch_append(p, batch, st) != cudaSuccess) return EKV_ERR_CUDA;
-  note_launch(st, false);
+  note_launch(st, kAfterAppend);
   return EKV_OK;
 }
 
@@ -541,7 +546,7 @@ ekv_status ekv_prefill_attention(ekv_ctx* c, const void* q, const void* ws_k, co
   p.err = c->err;
   const cudaError_t e = c->variant == 1 ? launch_prefill(p, D, max_len, st) : launch_prefill_tc05(p, D, max_len, st);
   if (e != cudaSuccess) return EKV_ERR_CUDA;
-  note_launch(st, false);
+  note_launch(st, kAfterReader);
   return EKV_OK;
 }
 

@@ -1,7 +1,7 @@
 // gather_demote.cu -- compact-prefill gather and TARGET -> compact demotion kernels.
 //
 // All are pure HBM streaming. Gather: one CTA per page, 16-byte vector loads issued
-// all before the first use. Mode transitions (demotion to E4M3 or BASE, promotion):
+// all before the first store. Mode transitions (demotion to E4M3 or BASE, promotion):
 // four persistent CTAs per SM, each with a ring of whole pages in shared memory.
 #include "common.cuh"
 #include "gather_demote.cuh"
@@ -14,8 +14,18 @@ namespace ekv {
 // ws_k[w] = K page (bits); ws_v[w] = TARGET page (bits),
 // fp16_rn(fp32_rn(E4M3(code) * s)) (fp16(E4M3(code)) when apply_scale == 0), or for a
 // BASE page the fp16 word (byte << 8) (ElasticKV App. B.3; exact, no scale).
-__global__ void __launch_bounds__(256)
+//
+// One CTA per workspace page: every load of the page (K, then V or its codes and
+// scales) is issued before the first store. Under a programmatic launch (p.pdl) the CTA
+// signals its dependents at once and makes all those loads before griddepcontrol.wait,
+// then writes the workspace after it: a gather that follows another gather (the chunks
+// of one prefill admission) streams its pages in while the previous one drains.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherVec = 8;                     // uint4 per thread: up to 32 KiB per fp16 page
+
+__global__ void __launch_bounds__(kGatherThreads)
 gather_kernel(const GatherParams p, const GatherRanges r) {
+  if (p.pdl) griddep_launch_dependents();
   const int i = blockIdx.x;                       // page index within this launch
   int k = 0;
   while (k + 1 < r.n && r.off[k + 1] <= i) ++k;   // ranges are few (<= kMaxRanges)
@@ -26,8 +36,8 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
   uint4* wk = reinterpret_cast<uint4*>(p.ws_k + (size_t)w * n_elem);
   uint4* wv = reinterpret_cast<uint4*>(p.ws_v + (size_t)w * n_elem);
   const int nvec16 = n_elem * 2 / 16;             // uint4 per fp16 page
+  const int nvec8 = n_elem / 16;                  // uint4 per byte page
   const int tid = threadIdx.x;
-  if (tid == 0) p.ws_indices[w] = w;
   int mode = 0;
   int detail = (page < 0 || page >= p.num_pages) ? EKV_DETAIL_PAGE_ID : EKV_DETAIL_NONE;
   int loc = 2 * page;                             // value location (half-slot index)
@@ -56,94 +66,86 @@ gather_kernel(const GatherParams p, const GatherRanges r) {
     }
   }
   if (detail != EKV_DETAIL_NONE) {
-    if (tid == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, detail, w);
-    for (int v = tid; v < nvec16; v += 256) {
+    if (p.pdl) griddep_wait();                    // writes only after the preceding kernel
+    if (tid == 0) {
+      p.ws_indices[w] = w;
+      report_error(p.err, EKV_ERR_DEVICE_CHECK, detail, w);
+    }
+    for (int v = tid; v < nvec16; v += kGatherThreads) {
       wk[v] = make_uint4(0, 0, 0, 0);
       wv[v] = make_uint4(0, 0, 0, 0);
     }
     return;
   }
-  // K: bit copy
+  // loads: the K page, then the value page (a TARGET page at slot loc / 2; a compact or
+  // BASE page in half loc % 2 of that slot) and, for codes, the KV heads' scales
   const uint4* sk = reinterpret_cast<const uint4*>(p.k_pages + (size_t)page * n_elem);
-  constexpr int kVecPerThread = 8;                // up to 32 KiB per page
-  {
-    uint4 buf[kVecPerThread];
+  const uint4* sv = reinterpret_cast<const uint4*>(p.v_pages + (size_t)(loc >> 1) * p.v_page_stride +
+                                                   (size_t)(loc & 1) * n_elem);
+  uint4 kb[kGatherVec], vb[kGatherVec];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int v = tid + u * 256;
-      if (v < nvec16) buf[u] = __ldg(sk + v);
-    }
+  for (int u = 0; u < kGatherVec; ++u) {
+    const int v = tid + u * kGatherThreads;
+    if (v < nvec16) kb[u] = __ldg(sk + v);
+  }
+  const int nv = mode == EKV_MODE_TARGET_FP16 ? nvec16 : nvec8;
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int v = tid + u * 256;
-      if (v < nvec16) wk[v] = buf[u];
+  for (int u = 0; u < kGatherVec; ++u) {
+    const int v = tid + u * kGatherThreads;
+    if (v < nv) vb[u] = __ldg(sv + v);
+  }
+  float sc[kGatherVec / 2];                       // E4M3: the scale of each code vector's head
+#pragma unroll
+  for (int u = 0; u < kGatherVec / 2; ++u) {
+    const int v = tid + u * kGatherThreads;
+    sc[u] = 1.f;
+    if (mode == EKV_MODE_COMPACT_E4M3 && p.apply_scale && v < nvec8) {
+      const int head = ((v * 16) / p.D) % p.Hkv;  // 16 codes of one head row (D >= 64)
+      sc[u] = p.scale_mode == EKV_SCALE_PER_TENSOR ? __ldg(p.v_scales)
+                                                   : __ldg(p.v_scales + (size_t)page * p.Hkv + head);
     }
   }
-  // a TARGET page at slot loc / 2; a compact or BASE page in half loc % 2 of that slot
-  const uint8_t* vsrc = p.v_pages + (size_t)(loc >> 1) * p.v_page_stride + (size_t)(loc & 1) * n_elem;
-  if (mode == 0) {
-    const uint4* sv = reinterpret_cast<const uint4*>(vsrc);
-    uint4 buf[kVecPerThread];
+  if (p.pdl) griddep_wait();                      // the workspace is written after it
+  if (tid == 0) p.ws_indices[w] = w;
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int v = tid + u * 256;
-      if (v < nvec16) buf[u] = __ldg(sv + v);
-    }
+  for (int u = 0; u < kGatherVec; ++u) {
+    const int v = tid + u * kGatherThreads;
+    if (v < nvec16) wk[v] = kb[u];
+  }
+  if (mode == EKV_MODE_TARGET_FP16) {             // bit copy
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-      const int v = tid + u * 256;
-      if (v < nvec16) wv[v] = buf[u];
+    for (int u = 0; u < kGatherVec; ++u) {
+      const int v = tid + u * kGatherThreads;
+      if (v < nvec16) wv[v] = vb[u];
     }
     return;
   }
-  // E4M3 or BASE: 16 bytes per uint4, all in one head row (D >= 64)
-  const int nvec8 = n_elem / 16;
-  const uint4* sv = reinterpret_cast<const uint4*>(vsrc);
-  constexpr int kCodeVecPerThread = 4;            // up to 16 KiB of codes
-  uint4 buf[kCodeVecPerThread];
+  // E4M3 or BASE: 16 codes per uint4, all in one head row (D >= 64) -> 2 uint4 of fp16
 #pragma unroll
-  for (int u = 0; u < kCodeVecPerThread; ++u) {
-    const int v = tid + u * 256;
-    if (v < nvec8) buf[u] = __ldg(sv + v);
-  }
-  if (mode == EKV_MODE_BASE) {                     // high byte in place, low byte zero
-#pragma unroll
-    for (int u = 0; u < kCodeVecPerThread; ++u) {
-      const int v = tid + u * 256;
-      if (v >= nvec8) continue;
-      const uint32_t words[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
-      uint32_t outw[8];
+  for (int u = 0; u < kGatherVec / 2; ++u) {
+    const int v = tid + u * kGatherThreads;
+    if (v >= nvec8) continue;
+    const uint32_t words[4] = {vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+    uint32_t outw[8];
+    if (mode == EKV_MODE_BASE) {                  // high byte in place, low byte zero
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         outw[2 * q] = __byte_perm(words[q], 0u, 0x1404);       // {0, b0, 0, b1}
         outw[2 * q + 1] = __byte_perm(words[q], 0u, 0x3424);   // {0, b2, 0, b3}
       }
-      wv[2 * v] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-      wv[2 * v + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-    }
-    return;
-  }
+    } else {
 #pragma unroll
-  for (int u = 0; u < kCodeVecPerThread; ++u) {
-    const int v = tid + u * 256;
-    if (v >= nvec8) continue;
-    const int head = ((v * 16) / p.D) % p.Hkv;
-    float s = 1.f;
-    if (p.apply_scale)
-      s = p.scale_mode == EKV_SCALE_PER_TENSOR ? __ldg(p.v_scales) : __ldg(p.v_scales + (size_t)page * p.Hkv + head);
-    const uint32_t words[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
-    uint32_t outw[8];
+      for (int q = 0; q < 4; ++q) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint16_t two = (uint16_t)(words[q] >> (16 * hh));
-        __half2 hv = e4m3x2_to_half2(two);
-        if (p.apply_scale) {
-          const float2 f = __half22float2(hv);
-          hv = __halves2half2(__float2half_rn(__fmul_rn(f.x, s)), __float2half_rn(__fmul_rn(f.y, s)));
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint16_t two = (uint16_t)(words[q] >> (16 * hh));
+          __half2 hv = e4m3x2_to_half2(two);
+          if (p.apply_scale) {
+            const float2 f = __half22float2(hv);
+            hv = __halves2half2(__float2half_rn(__fmul_rn(f.x, sc[u])), __float2half_rn(__fmul_rn(f.y, sc[u])));
+          }
+          outw[q * 2 + hh] = *reinterpret_cast<uint32_t*>(&hv);
         }
-        outw[q * 2 + hh] = *reinterpret_cast<uint32_t*>(&hv);
       }
     }
     wv[2 * v] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
@@ -496,8 +498,21 @@ cudaError_t launch_append(const AppendParams& p, int batch, cudaStream_t st) {
 
 cudaError_t launch_gather(const GatherParams& p, const GatherRanges& r, int pages, cudaStream_t st) {
   if (pages <= 0) return cudaSuccess;
-  gather_kernel<<<pages, 256, 0, st>>>(p, r);
-  return cudaGetLastError();
+  if (!p.pdl) {
+    gather_kernel<<<pages, kGatherThreads, 0, st>>>(p, r);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pages);
+  cfg.blockDim = dim3(kGatherThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_kernel, p, r);
 }
 
 }  // namespace ekv

@@ -38,6 +38,10 @@ struct GatherParams {
   int num_v_slots;                // slots of v_pages (elastic layout only)
   const int32_t* boundaries;      // [B][2] T-B-T boundaries or null (elastic layout only)
   int has_base;                   // 0: every page TARGET (elastic layout only)
+  // 1: launched with programmatic serialization. Before its griddepcontrol.wait the
+  // kernel reads only the block tables, page metadata, scales and pool pages; it writes
+  // the workspace, the indices and the error word after it.
+  int pdl;
 };
 
 // Page-mode transitions run by the same streaming kernel.

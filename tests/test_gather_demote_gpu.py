@@ -145,3 +145,85 @@ def test_demote_then_gather_round_trip(ekv_lib, torch_cuda):
     for p in range(P):
         if m[p] == 0:
             assert np.array_equal(ws_v[p].view(np.uint16), x[p].view(np.uint16))
+
+
+def test_gather_chunks_back_to_back_under_pdl(ekv_lib, torch_cuda):
+    """Gather calls back to back with the programmatic launch switched on (each next call
+    reads its pages while the previous one drains): chunks into disjoint workspace
+    regions and into the same region, a demotion and a cache-writer append in between
+    (after which the gather runs in plain stream order); every call bit-exact against the
+    oracle on the state it must see. More than 128 ranges per call also makes one call
+    launch several kernels back to back."""
+    torch = torch_cuda
+    from oracle import writer as ow
+    lens = [16 * 20 + 3] * 6 + [16 * 2] * 200
+    case = wl.make_decode_case(lens, 16, 8, 128, v_format="mixed", scale_mode=1, seed=27, poison=False,
+                               pool_pages=sum((l + 15) // 16 for l in lens) + 2, p_compact=0.4, p_base=0.2)
+    d = to_device(case)
+    H, D, B = 8, 128, case.batch
+    ctx = ekv_lib.Context(16, H, D, B, pdl=True)
+    chunks = [np.array([[b, 0, 21]]) for b in range(6)] + [np.array([[b, 0, 2] for b in range(6, 206)])]
+    sizes = [int(c[:, 2].sum()) for c in chunks]
+    W = sum(sizes)
+    ws_k = torch.full((W, 16, H, D), float("nan"), dtype=torch.float16, device="cuda")
+    ws_v = torch.full_like(ws_k, float("nan"))
+    idx = torch.full((W,), -1, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    n_elem = 16 * H * D
+
+    def gather(pr, off, n):
+        ekv_lib.ekv_gather_prefill(ctx.handle, d.k_pages, d.v_pages, case.v_page_stride, case.num_pages,
+                                   d.v_scales, 1, d.page_mode, 0, d.block_table, case.block_table.shape[1], B, pr,
+                                   ws_k[off:off + n], ws_v[off:off + n], idx[off:off + n], n, 1, st)
+
+    def check(k, v, pr, off, n, pool_v, pool_k, modes, scales):
+        rk, rv, ri = og.gather_prefill(pool_k, pool_v, scales, 1, modes, 0, case.block_table, pr)
+        assert np.array_equal(k[off:off + n].view(np.uint16), rk.view(np.uint16))
+        assert np.array_equal(v[off:off + n].view(np.uint16), rv.view(np.uint16))
+
+    for rep in range(20):                               # disjoint regions, no sync in between
+        off = 0
+        for pr, n in zip(chunks, sizes):
+            gather(pr, off, n)
+            off += n
+    torch.cuda.synchronize()
+    assert ctx.error() == (0, 0)
+    k, v = ws_k.cpu().numpy(), ws_v.cpu().numpy()
+    off = 0
+    for pr, n in zip(chunks, sizes):
+        check(k, v, pr, off, n, case.v_pages, case.k_pages, case.page_mode, case.v_scales)
+        off += n
+    assert np.array_equal(idx.cpu().numpy(), np.concatenate([np.arange(n) for n in sizes]))
+    # the same region rewritten by consecutive calls: the last one wins
+    for pr in chunks[:6]:
+        gather(pr, 0, 21)
+    torch.cuda.synchronize()
+    check(ws_k.cpu().numpy(), ws_v.cpu().numpy(), chunks[5], 0, 21, case.v_pages, case.k_pages,
+          case.page_mode, case.v_scales)
+    # a demotion of sequence 0's TARGET pages, then at once a gather of them
+    pages0 = case.block_table[0, :21]
+    ids = np.array([p for p in pages0 if case.page_mode[p] == 0], np.int32)
+    gather(chunks[1], 0, 21)
+    ekv_lib.ekv_demote_pages(ctx.handle, d.v_pages, case.v_page_stride, case.num_pages,
+                             torch.from_numpy(ids).cuda(), len(ids), d.page_mode, d.v_scales, st)
+    gather(chunks[0], 0, 21)
+    torch.cuda.synchronize()
+    assert ctx.error() == (0, 0)
+    rv_pool, rm, rs = odm.demote_pages(case.v_pages, ids, case.page_mode, case.v_scales, H, D)
+    check(ws_k.cpu().numpy(), ws_v.cpu().numpy(), chunks[0], 0, 21, rv_pool, case.k_pages, rm, rs)
+    # a cache-writer append into sequence 1's last page, then at once a gather of it
+    pos = np.full(B, -1, np.int32)
+    pos[1] = lens[1] - 1                                # rewrite the last token of sequence 1
+    kn = np.random.default_rng(28).standard_normal((B, H, D)).astype(np.float16)
+    vn = np.random.default_rng(29).standard_normal((B, H, D)).astype(np.float16)
+    gather(chunks[2], 0, 21)
+    ekv_lib.ekv_append_kv(ctx.handle, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(), d.k_pages,
+                          d.v_pages, case.v_page_stride, case.num_pages, d.v_scales, 1, d.page_mode, 0,
+                          d.block_table, case.block_table.shape[1], torch.from_numpy(pos).cuda(), B, st)
+    gather(chunks[1], 0, 21)
+    torch.cuda.synchronize()
+    assert ctx.error() == (0, 0)
+    k2, v2 = ow.append_token(case.k_pages, rv_pool, rs, 1, rm, 0, case.block_table, pos, kn, vn)
+    check(ws_k.cpu().numpy(), ws_v.cpu().numpy(), chunks[1], 0, 21, v2, k2, rm, rs)
+    assert n_elem == 16 * H * D
+    ctx.close()
