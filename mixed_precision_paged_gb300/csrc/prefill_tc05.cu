@@ -24,9 +24,11 @@
 //                over the first half of S's columns, and at the end normalise O and write
 //                out and lse.
 // Tensor memory, tile t: S/P at 256t (128 columns), O at 256t + 128 (D fp32 columns).
-// The MMA warp issues S of block j + 1 over P of block j only after O += P_j V_j has
-// completed; the softmax of block j + 1 therefore never waits for the tensor core, and
-// may rescale O at any time before it hands over P.
+// The MMA warp issues S of block j + 1 over P of block j right behind O += P_j V_j (the
+// tensor core runs one thread's MMAs in issue order, so P_j is read before S_{j+1}
+// overwrites it); the commit that signals S_{j+1} arrives only when every earlier MMA,
+// O += P_j V_j included, has completed, so the softmax of block j + 1 may rescale O at
+// any time before it hands over P.
 // The instruction stream of the MMA warp is the scarce resource: one tcgen05.mma or
 // tcgen05.commit issues every ~45 cycles per SM whatever its size, so the MMAs are the
 // largest the tensor memory allows (N = 128 for S, N = D for O) and their descriptors are
@@ -52,6 +54,7 @@ constexpr int kQRows = 128;                 // rows of a query tile (MMA M)
 constexpr int kKB = 128;                    // keys per K / V block (S's N)
 constexpr int kTThreads = 384;
 constexpr float kRebase = 8.f;              // log2 growth of the max that forces a rescale
+constexpr int kL2Ahead = 3;                 // key/value blocks prefetched into L2 ahead of the ring
 
 template <int D>
 struct TcCfg {
@@ -69,8 +72,8 @@ struct TcBars {
   uint64_t kv_full[NS];          // TMA bytes landed
   uint64_t kv_empty[NS];         // the MMAs reading the stage have completed
   uint64_t s_full[2];            // [tile]: S of the next block written
-  uint64_t p_full[2];            // [tile]: P written, S read (128 arrivals)
-  uint64_t pv_done[2];           // [tile]: O += P V of the block completed
+  uint64_t p_full[2];            // [tile]: P written, S read (one arrival per softmax warp)
+  uint64_t pv_done[2];           // [tile]: the tile's last O += P V completed (one phase)
   uint32_t tmem_base;
   int abort;
 };
@@ -88,6 +91,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0 && (*abort || globaltimer_ns() - t0 > kWaitTimeoutNs)) return false;
   }
+}
+
+// Bulk tensor prefetch of one box into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* tm, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
 }
 
 __device__ __forceinline__ void give_up(int* err, volatile int* abort) {
@@ -142,65 +153,62 @@ __device__ __forceinline__ void tst16(uint32_t taddr, const uint32_t (&r)[16]) {
       : "memory");
 }
 
-// Row max of one 128-column S block (tensor memory at t_s), 64 columns per load wait;
-// with MASK, columns whose key k0 + col follows the query prow count as -inf.
-template <bool MASK>
-__device__ __forceinline__ float block_max(uint32_t t_s, int k0, int prow) {
-  float mx = -INFINITY;
-#pragma unroll 1
-  for (int c = 0; c < kKB / 32; c += 2) {
-    uint32_t a[2][32];
-    tc05::ld32(t_s + 32 * c, a[0]);
-    tc05::ld32(t_s + 32 * c + 32, a[1]);
-    tc05::wait_ld();
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      float x[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        x[e] = (MASK && k0 + 32 * (c + h2) + e > prow) ? -INFINITY : __uint_as_float(a[h2][e]);
-      float mg[4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const float* y = x + 8 * g;
-        mg[g] = fmaxf(max3f(max3f(y[0], y[1], y[2]), y[3], y[4]), max3f(y[5], y[6], y[7]));
-      }
-      mx = max3f(mx, max3f(mg[0], mg[1], mg[2]), mg[3]);
-    }
-  }
-  return mx;
+// Warp-wide load of 16 columns (thread t: lane base + t).
+__device__ __forceinline__ void tld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
 }
 
-// P = exp2(S * qs + nm) of one S block as fp16 over the first half of its columns (chunk
-// c writes columns 16c.., whose S values chunks <= c have already read); returns the sum
-// of the fp32 exponentials. MASK as for block_max.
+// The S row of one 128-key block, read from tensor memory into registers once: with
+// MASK, keys k0 + col after the query prow become -inf. Returns the row max (raw score).
 template <bool MASK>
-__device__ __forceinline__ float block_exp(uint32_t t_s, int k0, int prow, float qs, float nm) {
-  float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-  for (int c = 0; c < kKB / 32; c += 2) {
-    uint32_t a[2][32];
-    tc05::ld32(t_s + 32 * c, a[0]);
-    tc05::ld32(t_s + 32 * c + 32, a[1]);
-    tc05::wait_ld();
+__device__ __forceinline__ float row_in_regs(uint32_t t_s, int k0, int prow, uint32_t (&a)[4][32]) {
+  tc05::ld32(t_s, a[0]);
+  tc05::ld32(t_s + 32, a[1]);
+  tc05::ld32(t_s + 64, a[2]);
+  tc05::ld32(t_s + 96, a[3]);
+  tc05::wait_ld();
+  float mg[4];
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      uint32_t pk[16];
+  for (int c = 0; c < 4; ++c) {
+    if (MASK) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        float a0, a1;
-        ffma2(a0, a1, __uint_as_float(a[h2][2 * e]), __uint_as_float(a[h2][2 * e + 1]), qs, qs, nm, nm);
-        if (MASK) {
-          const int col = k0 + 32 * (c + h2) + 2 * e;
-          if (col > prow) a0 = -INFINITY;
-          if (col + 1 > prow) a1 = -INFINITY;
-        }
-        const float p0 = ex2f(a0), p1 = ex2f(a1);
-        fadd2(la[e & 3], lb[e & 3], p0, p1);
-        pk[e] = pack_half2(p0, p1);
-      }
-      tst16(t_s + 16 * (c + h2), pk);
+      for (int e = 0; e < 32; ++e)
+        if (k0 + 32 * c + e > prow) a[c][e] = __float_as_uint(-INFINITY);
     }
+    float m8[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t* y = a[c] + 8 * g;
+      m8[g] = fmaxf(max3f(max3f(__uint_as_float(y[0]), __uint_as_float(y[1]), __uint_as_float(y[2])),
+                          __uint_as_float(y[3]), __uint_as_float(y[4])),
+                    max3f(__uint_as_float(y[5]), __uint_as_float(y[6]), __uint_as_float(y[7])));
+    }
+    mg[c] = max3f(m8[0], m8[1], fmaxf(m8[2], m8[3]));
+  }
+  return max3f(mg[0], mg[1], fmaxf(mg[2], mg[3]));
+}
+
+// P = exp2(S * qs + nm) of the row held in registers, as fp16 pairs over the first 64
+// tensor-memory columns of the block (S is no longer read there); returns the sum of the
+// fp32 exponentials.
+__device__ __forceinline__ float row_exp_store(uint32_t t_s, float qs, float nm, uint32_t (&a)[4][32]) {
+  float la[4] = {0.f, 0.f, 0.f, 0.f}, lb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float a0, a1;
+      ffma2(a0, a1, __uint_as_float(a[c][2 * e]), __uint_as_float(a[c][2 * e + 1]), qs, qs, nm, nm);
+      const float p0 = ex2f(a0), p1 = ex2f(a1);
+      fadd2(la[e & 3], lb[e & 3], p0, p1);
+      a[c][e] = pack_half2(p0, p1);                 // a[c][2e], a[c][2e + 1] already read
+    }
+    tst16(t_s + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(&a[c][0]));
   }
   fadd2(la[0], lb[0], la[2], lb[2]);
   fadd2(la[1], lb[1], la[3], lb[3]);
@@ -257,7 +265,7 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], kQRows);
+      mbar_init(&bars->p_full[t], kQRows / 32);
       mbar_init(&bars->pv_done[t], 1);
     }
     bars->abort = 0;
@@ -285,6 +293,9 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars->kv_full[stage], C::IB);
           tma_load_4d(dst, is_v ? &tv : &tk, 0, tok0 + j * kKB, 0, h, &bars->kv_full[stage]);
+          // the blocks kL2Ahead further on go to L2 now, so that their loads into the ring,
+          // issued once stages free up, come from L2
+          if (j + kL2Ahead < n) tma_prefetch_l2_4d(is_v ? &tv : &tk, 0, tok0 + (j + kL2Ahead) * kKB, 0, h);
         }
         if (is_v && j == n - 1 && zr < kKB) {
           ok = __all_sync(0xffffffffu, wait_bar(&bars->kv_full[stage], phase, abort));
@@ -315,77 +326,97 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = tc05::idesc_f16_f32(kQRows, kKB, false);
-      constexpr uint32_t idO = tc05::idesc_f16_f32(kQRows, D, true);
-      constexpr uint32_t HI = tc05::sdesc_hi(1024);        // 8-row groups 1024 B apart
-      const int nt[2] = {nt0, nt1};
-      // descriptor low words: Q tile 0, K-major and V (N-major) views of ring stage 0
-      const uint32_t q_lo = tc05::sdesc_lo(smem_u32(sQ), 16);
-      const uint32_t k_lo = tc05::sdesc_lo(smem_u32(sKV), 16);
-      const uint32_t v_lo = tc05::sdesc_lo(smem_u32(sKV), kKB * 128);
-      // ring cursors of the K items (2j) and the V items (2j + 1)
-      int ks = 0, vs = 1;
-      uint32_t kp = 0, vp = 0;
-      auto adv2 = [&](int& s, uint32_t& ph) {
-        s += 2;
-        if (s >= NS) {
-          s -= NS;
-          ph ^= 1u;
-        }
-      };
-      auto issue_s = [&](int t) {                          // S_t = Q_t K^T from stage ks
-        const uint32_t qa = q_lo + t * (C::QB >> 4), ka = k_lo + ks * (C::IB >> 4);
+    // The whole warp runs the control flow and computes the descriptors (warp-uniform
+    // values); one elected lane issues each group of MMAs and commits.
+    constexpr uint32_t idS = tc05::idesc_f16_f32(kQRows, kKB, false);
+    constexpr uint32_t idO = tc05::idesc_f16_f32(kQRows, D, true);
+    constexpr uint32_t HI = tc05::sdesc_hi(1024);          // 8-row groups 1024 B apart
+    const int nt[2] = {nt0, nt1};
+    // descriptor low words: Q tile 0, K-major and V (N-major) views of ring stage 0
+    const uint32_t q_lo = tc05::sdesc_lo(smem_u32(sQ), 16);
+    const uint32_t k_lo = tc05::sdesc_lo(smem_u32(sKV), 16);
+    const uint32_t v_lo = tc05::sdesc_lo(smem_u32(sKV), kKB * 128);
+    // ring cursors of the K items (2j) and the V items (2j + 1)
+    int ks = 0, vs = 1;
+    uint32_t kp = 0, vp = 0;
+    auto adv2 = [&](int& s, uint32_t& ph) {
+      s += 2;
+      if (s >= NS) {
+        s -= NS;
+        ph ^= 1u;
+      }
+    };
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_bar(bar, parity, abort));
+    };
+    auto issue_s = [&](int t) {                            // S_t = Q_t K^T from stage ks
+      const uint32_t qa = q_lo + t * (C::QB >> 4), ka = k_lo + ks * (C::IB >> 4);
+      const uint32_t d = tbase + t * 256;
+      if (tc05::elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc05::mma_ss(tbase + t * 256, tc05::sdesc_join(qa + (((k >> 2) * (kQRows * 128) + (k & 3) * 32) >> 4), HI),
+          tc05::mma_ss(d, tc05::sdesc_join(qa + (((k >> 2) * (kQRows * 128) + (k & 3) * 32) >> 4), HI),
                        tc05::sdesc_join(ka + (((k >> 2) * (kKB * 128) + (k & 3) * 32) >> 4), HI), idS, k > 0);
         tc05::commit(&bars->s_full[t]);
-      };
-      bool ok = wait_bar(&bars->q_full, 0, abort) && wait_bar(&bars->kv_full[ks], kp, abort);
-      if (ok) {
-        tc05::fence_after_sync();
-        for (int t = 0; t < 2; ++t)
-          if (nt[t] > 0) issue_s(t);
-        tc05::commit(&bars->kv_empty[ks]);
-        adv2(ks, kp);
       }
-      for (int j = 0; ok && j < n; ++j) {
-        ok = (j == n - 1 && zr < kKB) ? wait_bar(&bars->v_fixed, 0, abort) : wait_bar(&bars->kv_full[vs], vp, abort);
+      __syncwarp();
+    };
+    auto commit_one = [&](uint64_t* bar) {
+      if (tc05::elect_one()) tc05::commit(bar);
+      __syncwarp();
+    };
+    bool ok = wait_all(&bars->q_full, 0) && wait_all(&bars->kv_full[ks], kp);
+    if (ok) {
+      tc05::fence_after_sync();
+      for (int t = 0; t < 2; ++t)
+        if (nt[t] > 0) issue_s(t);
+      commit_one(&bars->kv_empty[ks]);
+      adv2(ks, kp);
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      ok = (j == n - 1 && zr < kKB) ? wait_all(&bars->v_fixed, 0) : wait_all(&bars->kv_full[vs], vp);
+      if (!ok) break;
+      tc05::fence_after_sync();
+      const uint32_t va = v_lo + vs * (C::IB >> 4);
+      bool k_ready = false;
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (j >= nt[t]) continue;
+        // O_t += P_t V_j once the softmax has written P
+        ok = wait_all(&bars->p_full[t], j & 1);
         if (!ok) break;
         tc05::fence_after_sync();
-        const uint32_t va = v_lo + vs * (C::IB >> 4);
-        bool k_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nt[t]) continue;
-          // O_t += P_t V_j once the softmax has written P
-          ok = wait_bar(&bars->p_full[t], j & 1, abort);
-          if (!ok) break;
-          tc05::fence_after_sync();
-          const uint32_t pa = tbase + t * 256, od = tbase + t * 256 + 128;
+        const uint32_t pa = tbase + t * 256, od = tbase + t * 256 + 128;
+        const bool acc0 = j > 0;
+        if (tc05::elect_one()) {
 #pragma unroll
           for (int k = 0; k < kKB / 16; ++k)
-            tc05::mma_ts(od, pa + 8 * k, tc05::sdesc_join(va + k * (2048 >> 4), HI), idO, j > 0 || k > 0);
-          tc05::commit(&bars->pv_done[t]);
-          if (j + 1 < nt[t]) {
-            // S_t of block j + 1 overwrites P_t: after O_t += P_t V_j has completed
-            ok = (k_ready || wait_bar(&bars->kv_full[ks], kp, abort)) && wait_bar(&bars->pv_done[t], j & 1, abort);
-            if (!ok) break;
-            k_ready = true;
-            tc05::fence_after_sync();
-            issue_s(t);
-          }
+            tc05::mma_ts(od, pa + 8 * k, tc05::sdesc_join(va + k * (2048 >> 4), HI), idO, acc0 || k > 0);
+          if (j + 1 == nt[t]) tc05::commit(&bars->pv_done[t]);   // the tile's last O += P V
         }
-        if (!ok) break;
-        tc05::commit(&bars->kv_empty[vs]);
-        adv2(vs, vp);
-        if (j + 1 < n) {
-          tc05::commit(&bars->kv_empty[ks]);
-          adv2(ks, kp);
+        __syncwarp();
+        if (j + 1 < nt[t]) {
+          // S_t of block j + 1 overwrites P_t. It is issued at once, behind O_t += P_t V_j:
+          // the tensor core runs the MMAs of this thread in issue order, so P_t is read
+          // before it is overwritten, and the commit after S_t (s_full) arrives only
+          // once every MMA issued before it, O_t += P_t V_j included, has completed.
+          ok = k_ready || wait_all(&bars->kv_full[ks], kp);
+          if (!ok) break;
+          k_ready = true;
+          tc05::fence_after_sync();
+          issue_s(t);
         }
       }
-      if (!ok) give_up(p.err, abort);
-      tc05::commit(&bars->mma_final);
+      if (!ok) break;
+      commit_one(&bars->kv_empty[vs]);
+      adv2(vs, vp);
+      if (j + 1 < n) {
+        commit_one(&bars->kv_empty[ks]);
+        adv2(ks, kp);
+      }
+    }
+    if (!ok && lane == 0) give_up(p.err, abort);
+    commit_one(&bars->mma_final);
+    if (lane == 0) {
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(&bars->mma_final, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
       }
@@ -414,40 +445,45 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     bool ok = true;
     const uint32_t t_s = tbase + t * 256 + lanebase, t_o = tbase + t * 256 + 128 + lanebase;
     for (int j = 0; j < nmine; ++j) {
+      // S of block j is ready; O += P V of block j - 1 has completed too (the commit that
+      // signals S was issued after it)
       ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full[t], j & 1, abort));
       if (!ok) break;
       tc05::fence_after_sync();
       const int k0 = j * kKB;
       const bool diag = k0 + kKB - 1 > q0 + t * kQRows;   // the block reaches past some row
-      const float mx = diag ? block_max<true>(t_s, k0, prow) : block_max<false>(t_s, k0, prow);
+      uint32_t sv[4][32];
+      const float mx = diag ? row_in_regs<true>(t_s, k0, prow, sv) : row_in_regs<false>(t_s, k0, prow, sv);
       const float m_new = fmaxf(m_ref, mx * qs);
       const bool need = m_new > m_ref + kRebase;
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2f(m_ref - m_new) : 1.f;
-        // O holds blocks < j, all complete (S of this block was issued after them)
+        // O holds blocks < j, all complete (S of this block was committed after them)
         if (j > 0) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tc05::ld32(t_o + 32 * c, o);
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tld16(t_o + 16 * c, o);
             tc05::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc05::st32(t_o + 32 * c, o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tst16(t_o + 16 * c, o);
           }
         }
         l *= alpha;
         if (need) m_ref = m_new;
       }
-      l += diag ? block_exp<true>(t_s, k0, prow, qs, -m_ref) : block_exp<false>(t_s, k0, prow, qs, -m_ref);
+      l += row_exp_store(t_s, qs, -m_ref, sv);
       tc05::wait_st();
       tc05::fence_before_sync();
-      mbar_arrive(&bars->p_full[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[t]);      // one arrival per warp
     }
     if (!ok && lane == 0) give_up(p.err, abort);
     if (ok && nmine > 0) {
-      // the last O += P V of the tile (its commit covers every earlier one)
-      ok = __all_sync(0xffffffffu, wait_bar(&bars->pv_done[t], (nmine - 1) & 1, abort));
+      // the last O += P V of the tile (its commit, the only one on pv_done, covers every
+      // earlier MMA)
+      ok = __all_sync(0xffffffffu, wait_bar(&bars->pv_done[t], 0, abort));
       if (!ok && lane == 0) give_up(p.err, abort);
     }
     if (ok && nmine > 0) {
