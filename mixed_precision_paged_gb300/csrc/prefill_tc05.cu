@@ -54,7 +54,6 @@ constexpr int kQRows = 128;                 // rows of a query tile (MMA M)
 constexpr int kKB = 128;                    // keys per K / V block (S's N)
 constexpr int kTThreads = 384;
 constexpr float kRebase = 8.f;              // log2 growth of the max that forces a rescale
-constexpr int kL2Ahead = 3;                 // key/value blocks prefetched into L2 ahead of the ring
 
 template <int D>
 struct TcCfg {
@@ -91,14 +90,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0 && (*abort || globaltimer_ns() - t0 > kWaitTimeoutNs)) return false;
   }
-}
-
-// Bulk tensor prefetch of one box into L2 (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* tm, int c0, int c1, int c2, int c3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                   reinterpret_cast<uint64_t>(tm)),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
 }
 
 __device__ __forceinline__ void give_up(int* err, volatile int* abort) {
@@ -293,9 +284,6 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars->kv_full[stage], C::IB);
           tma_load_4d(dst, is_v ? &tv : &tk, 0, tok0 + j * kKB, 0, h, &bars->kv_full[stage]);
-          // the blocks kL2Ahead further on go to L2 now, so that their loads into the ring,
-          // issued once stages free up, come from L2
-          if (j + kL2Ahead < n) tma_prefetch_l2_4d(is_v ? &tv : &tk, 0, tok0 + (j + kL2Ahead) * kKB, 0, h);
         }
         if (is_v && j == n - 1 && zr < kKB) {
           ok = __all_sync(0xffffffffu, wait_bar(&bars->kv_full[stage], phase, abort));
