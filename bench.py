@@ -645,6 +645,51 @@ def run_prefill_only(args):
     ctx.close()
 
 
+def run_gather_only(args):
+    """The compact-prefill gather alone on the gather/demotion workload (16,384 pages in 4
+    chunks of 4,096 into one workspace, chunk calls back to back under programmatic
+    dependent launch, then in plain stream order); one JSON line (ms per 4 chunks, GB/s)."""
+    import torch
+    from mixed_precision_paged_gb300 import build
+    build.ensure_built()
+    from mixed_precision_paged_gb300 import ekv
+    from mixed_precision_paged_gb300 import roofline as rf
+    from mixed_precision_paged_gb300 import workloads as wl
+    gd = wl.device_gather_demote_case(seed=1004)
+    P, S, H, D = gd.k_pages.shape
+    ws_k = torch.empty((gd.ws_pages, S, H, D), dtype=torch.float16, device="cuda")
+    ws_v = torch.empty_like(ws_k)
+    idx = torch.empty((gd.ws_pages,), dtype=torch.int32, device="cuda")
+    bt = gd.block_table
+    res = {}
+    for name, pdl in (("pdl", True), ("plain", False)):
+        ctx = ekv.Context(H, H, D, 1, pdl=pdl)
+
+        def gather_all():
+            for pr in gd.chunks:
+                ekv.ekv_gather_prefill(ctx.handle, gd.k_pages, gd.v8_pages, gd.v8_pages.shape[1], P, gd.v_scales, 1,
+                                       None, 1, bt, bt.shape[1], bt.shape[0], pr, ws_k, ws_v, idx, gd.ws_pages)
+        for _ in range(args.warmup):
+            gather_all()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.steps):
+            gather_all()
+        e.record()
+        torch.cuda.synchronize()
+        res[name] = s.elapsed_time(e) / args.steps
+        res[name + "_device_error"] = list(ctx.error())
+        ctx.close()
+    gb = rf.gather_bytes(P, P, H, D, per_page_scales=True)
+    peaks, src = load_peaks()
+    print(json.dumps({"gather_only": "16,384 pages in 4 chunks of 4,096", "bytes": gb,
+                      "ms_pdl": res["pdl"], "GB/s_pdl": gb / res["pdl"] / 1e6,
+                      "ms_plain": res["plain"], "GB/s_plain": gb / res["plain"] / 1e6,
+                      "frac_of_measured_hbm_pdl": gb / res["pdl"] / 1e6 / peaks["hbm_gbs"], "peak_source": src,
+                      "device_error": [res["pdl_device_error"], res["plain_device_error"]]}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -662,6 +707,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--prefill-only", type=int, nargs=2, metavar=("PROMPTS", "TOKENS"),
                     help="time only the FP16 causal prefill on PROMPTS x TOKENS (profiling)")
+    ap.add_argument("--gather-only", action="store_true",
+                    help="time only the compact-prefill gather on its workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -669,6 +716,8 @@ def main():
         return run_reference(args)
     if args.prefill_only:
         return run_prefill_only(args)
+    if args.gather_only:
+        return run_gather_only(args)
 
     import torch
     import torch.distributed as dist
