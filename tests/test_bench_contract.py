@@ -33,3 +33,25 @@ def test_reference_arm_prints_one_json_line():
     assert e["value"] == d["value"] and e["unit"] == "GB/s"
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
 
+
+
+def test_traffic_is_taken_only_for_the_kernel_source_it_was_captured_on(tmp_path):
+    """roofline.traffic comes from profiles/traffic.json only when the entry's source hash is
+    the hash of the decode sources as the production library compiles them: blocks that only
+    the tests' library builds are left out of the hash (an #else branch is kept), every other
+    change to the sources changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = (b"a\n#ifdef EKV_TEST_WAIT_TIMEOUT\nx\n#endif\n\nb\n"
+           b"#ifdef EKV_TEST_WAIT_TIMEOUT\ny\n#else\nz\n#endif\nc\n")
+    assert bench._production_source(src) == b"a\nb\nz\nc\n"
+    assert bench._production_source(b"a\n#ifdef OTHER\nx\n#endif\n") == b"a\n#ifdef OTHER\nx\n#endif\n"
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["decode_split_mma"]
+    entry = rec["pages_shape"]
+    if entry["kernel_source_hash"] == bench.kernel_source_hash():
+        assert bench.profiled_traffic("pages_shape") == float(entry["traffic_bytes_per_launch"])
+    else:
+        assert bench.profiled_traffic("pages_shape") is None
+    for name, e in rec.items():
+        if e.get("kernel_source_hash") is None:
+            assert bench.profiled_traffic(name) is None
