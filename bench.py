@@ -805,6 +805,8 @@ def main():
     split_ms, split_n = ekv.ekv_profile_read(ctx.handle)
     ekv.ekv_profile_enable(ctx.handle, False)
     ekv.ekv_set_pdl(ctx.handle, int(pdl))
+    # what the same events cost around an empty launch of the split kernel's shape
+    floor_ms = ekv.ekv_profile_launch_floor(ctx.handle, 64, stream)
     err = ctx.error()
     if world > 1:
         t = torch.tensor([elapsed_ms], device="cuda")
@@ -925,7 +927,12 @@ def main():
                                          "achieved": achieved, "frac": achieved / hbm if achieved else None,
                                          "launch_mode": "each launch alone in plain stream order, between the "
                                                         "library's CUDA events on the launching stream (a "
-                                                        "separate pass after the timed region)"}},
+                                                        "separate pass after the timed region)",
+                                         "launch_floor_ms": floor_ms,
+                                         "launch_floor": "an empty kernel with the split kernel's grid, block, "
+                                                         "shared memory and parameters, between the same "
+                                                         "events, the stream kept busy so that the launches "
+                                                         "queue (ekv_profile_launch_floor)"}},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
                 "layer_chunks": [len(ls) for ls in chunks], "outputs_equal_device_run": e2e_same},

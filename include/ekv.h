@@ -365,6 +365,14 @@ ekv_status ekv_get_error(ekv_ctx* ctx, int* code, int* detail);
 ekv_status ekv_profile_enable(ekv_ctx* ctx, int enable);
 ekv_status ekv_profile_read(ekv_ctx* ctx, double* split_ms, long long* launches);
 
+/* The fixed cost of one timed launch, for reading the split-kernel times above: `reps`
+ * (1..1024) launches of an empty kernel with the split kernel's grid, block, dynamic
+ * shared memory (D = head_dim, E4M3 slots) and parameter size, each between two CUDA
+ * events on `stream` (NULL = the default stream) exactly as a profiled decode is. Writes
+ * the average milliseconds between the two events of one launch to *avg_ms. The kernel
+ * touches no memory. Synchronises the stream; EKV_ERR_CUDA on a CUDA failure. */
+ekv_status ekv_profile_launch_floor(ekv_ctx* ctx, int reps, void* stream, double* avg_ms);
+
 /* Consumer variant of this context. Decode: 0 (default) multiplies the QK and PV
  * tiles on the tensor cores (mma.sync f16 -> f32); 1 uses CUDA-core FP32 FMAs. Prefill
  * (ekv_prefill_attention): 0 runs on the fifth-generation tensor cores (tcgen05 MMA,

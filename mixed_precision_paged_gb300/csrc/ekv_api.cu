@@ -19,6 +19,34 @@ cudaError_t launch_split_simt(const CUtensorMap& tk, const CUtensorMap& t8, cons
                               const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st);
 cudaError_t launch_split_mma(const CUtensorMap& tk, const CUtensorMap& t8, const CUtensorMap& t16,
                              const DecodeParams& p, int D, int vmode, int grid, size_t smem, cudaStream_t st);
+
+// ------------------------------------------------------------- launch floor
+// An empty kernel with the split kernel's block, shared memory and parameter list: what
+// a timed launch costs before any work (ekv_profile_launch_floor).
+__global__ void __launch_bounds__(kThreads, 1)
+launch_floor_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                    const __grid_constant__ CUtensorMap, const DecodeParams) {}
+
+// One thread that returns `ns` nanoseconds after it starts: keeps the stream busy while
+// the host queues the timed launches behind it (bounded by construction).
+__global__ void hold_stream_kernel(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
+}
+
+static cudaError_t launch_floor(int grid, size_t smem, cudaStream_t st, int reps, cudaEvent_t* ev) {
+  cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(launch_floor_kernel));
+  if (e != cudaSuccess) return e;
+  hold_stream_kernel<<<1, 1, 0, st>>>(2000000ull + 20000ull * (uint64_t)reps);
+  CUtensorMap tm{};
+  DecodeParams p{};
+  for (int i = 0; i < reps; ++i) {
+    cudaEventRecord(ev[2 * i], st);
+    launch_floor_kernel<<<grid, kThreads, smem, st>>>(tm, tm, tm, p);
+    cudaEventRecord(ev[2 * i + 1], st);
+  }
+  return cudaGetLastError();
+}
 }  // namespace ekv
 
 using namespace ekv;
@@ -596,6 +624,32 @@ ekv_status ekv_profile_read(ekv_ctx* c, double* split_ms, long long* launches) {
   if (launches) *launches = (long long)c->ev_used;
   c->ev_used = 0;
   return EKV_OK;
+}
+
+ekv_status ekv_profile_launch_floor(ekv_ctx* c, int reps, void* stream, double* avg_ms) {
+  if (!c || !avg_ms || reps < 1 || reps > 1024) return EKV_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  DecodeParams p{};
+  p.batch = c->cfg.max_batch;
+  const size_t smem = split_layout(p, c->cfg.head_dim, kVE4M3, kAlgoMma);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<cudaEvent_t> ev(2 * (size_t)reps, nullptr);
+  ekv_status status = EKV_OK;
+  for (auto& e : ev)
+    if (cudaEventCreate(&e) != cudaSuccess) status = EKV_ERR_CUDA;
+  double ms = 0.0;
+  if (status == EKV_OK && (launch_floor(c->split_ctas, smem, st, reps, ev.data()) != cudaSuccess ||
+                           cudaStreamSynchronize(st) != cudaSuccess))
+    status = EKV_ERR_CUDA;
+  for (int i = 0; status == EKV_OK && i < reps; ++i) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, ev[2 * i], ev[2 * i + 1]) != cudaSuccess) status = EKV_ERR_CUDA;
+    ms += t;
+  }
+  for (auto& e : ev)
+    if (e) cudaEventDestroy(e);
+  if (status == EKV_OK) *avg_ms = ms / reps;
+  return status;
 }
 
 #ifdef EKV_TEST_WAIT_TIMEOUT

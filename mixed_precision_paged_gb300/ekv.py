@@ -48,7 +48,7 @@ EXPORTED = ["ekv_create", "ekv_destroy", "ekv_paged_decode", "ekv_gather_prefill
             "ekv_set_decode_variant", "ekv_query", "ekv_paged_decode_noalloc",
             "ekv_demote_pages_base", "ekv_promote_pages", "ekv_append_kv", "ekv_paged_decode_elastic",
             "ekv_transition_pages", "ekv_prefill_attention", "ekv_gather_prefill_elastic",
-            "ekv_set_pdl", "ekv_status_string"]
+            "ekv_set_pdl", "ekv_profile_launch_floor", "ekv_status_string"]
 
 
 class ekv_config(ctypes.Structure):
@@ -81,6 +81,7 @@ _lib.ekv_paged_decode_noalloc.argtypes = [_i, _i, _i, _vp, _vp, _vp, _ll, _i, _v
 _lib.ekv_get_error.argtypes = [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]
 _lib.ekv_profile_enable.argtypes = [_vp, _i]
 _lib.ekv_profile_read.argtypes = [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_ll)]
+_lib.ekv_profile_launch_floor.argtypes = [_vp, _i, _vp, ctypes.POINTER(ctypes.c_double)]
 _lib.ekv_set_decode_variant.argtypes = [_vp, _i]
 _lib.ekv_set_pdl.argtypes = [_vp, _i]
 _lib.ekv_query.argtypes = [_vp, ctypes.POINTER(_i), ctypes.POINTER(_i)]
@@ -268,6 +269,14 @@ def ekv_profile_read(ctx):
 
 def ekv_set_decode_variant(ctx, variant):
     _check(_lib.ekv_set_decode_variant(ctx, variant), "ekv_set_decode_variant")
+
+
+def ekv_profile_launch_floor(ctx, reps=64, stream=None):
+    """Average ms between the CUDA events of one empty launch shaped like the split kernel."""
+    ms = ctypes.c_double(0.0)
+    _check(_lib.ekv_profile_launch_floor(ctx, int(reps), _stream(stream), ctypes.byref(ms)),
+           "ekv_profile_launch_floor")
+    return ms.value
 
 
 def ekv_set_pdl(ctx, enable):

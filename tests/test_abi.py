@@ -45,6 +45,9 @@ def test_null_arguments_are_rejected_without_a_gpu(ekv_lib):
     assert L.ekv_demote_pages(None, None, 0, 0, None, 0, None, None, None) == ekv_lib.EKV_ERR_INVALID_ARG
     assert L.ekv_set_pdl(None, 1) == ekv_lib.EKV_ERR_INVALID_ARG
     assert L.ekv_set_decode_variant(None, 0) == ekv_lib.EKV_ERR_INVALID_ARG
+    ms = ctypes.c_double(-1.0)
+    assert L.ekv_profile_launch_floor(None, 8, None, ctypes.byref(ms)) == ekv_lib.EKV_ERR_INVALID_ARG
+    assert ms.value == -1.0
     assert L.ekv_destroy(None) == ekv_lib.EKV_OK
 
 

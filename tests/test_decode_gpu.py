@@ -151,6 +151,31 @@ def test_batch_larger_than_the_range_count(ekv_lib, torch_cuda, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("offset", [-1, 0, 1, 7, "2nv-1"])
+def test_cost_stream_around_the_range_count(ekv_lib, torch_cuda, variant, offset):
+    # The cost stream (T positions: pages + 2 per sequence start) is cut into one range per
+    # (CTA, page group) of ceil(T / nv) positions, so around T = nv the last ranges hold
+    # one position or none. Lengths are drawn so that T lands just around nv.
+    ctx0 = make_ctx(ekv_lib, wl.make_decode_case([16], 8, 8, 64, seed=1), variant)
+    _, nv = ekv_lib.ekv_query(ctx0.handle)              # 8 KV heads: one page group per CTA
+    batch = 24
+    target = 2 * nv - 1 if offset == "2nv-1" else nv + offset
+    pages = target - 2 * batch
+    rng = np.random.default_rng(70 + (0 if offset == "2nv-1" else offset + 2))
+    cuts = np.sort(rng.integers(0, pages + 1, size=batch - 1))
+    per_seq = np.diff(np.concatenate([[0], cuts, [pages]]))
+    lens = [int(n * 16 - (rng.integers(0, 16) if n > 0 else 0)) for n in per_seq]
+    assert sum((l + 15) // 16 for l in lens) + 2 * batch == target
+    case = wl.make_decode_case(lens, 32, 8, 64, v_format="mixed", scale_mode=1,
+                               pool_pages=pages + 3, seed=71)
+    ctx = make_ctx(ekv_lib, case, variant)
+    out, lse = gpu_decode(ctx, to_device(case))
+    ref_out, ref_lse = oracle_decode(case)
+    assert_close(out, lse, ref_out, ref_lse)
+    assert ctx.error() == (0, 0)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("fmt,scale_mode", [("fp16", 0), ("mixed", 1), ("e4m3", 0)])
 def test_scores_growing_along_the_sequence(ekv_lib, torch_cuda, variant, fmt, scale_mode):
     # keys scaled up page by page, so the page max of the scores keeps passing the running
@@ -255,6 +280,18 @@ def test_variants_agree(ekv_lib, torch_cuda):
     b, lb = gpu_decode(make_ctx(ekv_lib, case, 1), to_device(case))
     assert (a.float() - b.float()).abs().max().item() <= 2e-3
     assert (la - lb).abs().max().item() <= 1e-3
+
+
+def test_launch_floor(ekv_lib, torch_cuda):
+    # the empty launch of the split kernel's shape: a few microseconds between its events,
+    # far below one decode launch; bad repetition counts are refused
+    ctx = ekv_lib.Context(32, 8, 128, 32)
+    ms = ekv_lib.ekv_profile_launch_floor(ctx.handle, 16)
+    assert 0.0 < ms < 0.1
+    for reps in (0, 1025):
+        with pytest.raises(RuntimeError):
+            ekv_lib.ekv_profile_launch_floor(ctx.handle, reps)
+    assert ctx.error() == (0, 0)
 
 
 def test_explicit_sm_scale(ekv_lib, torch_cuda):
