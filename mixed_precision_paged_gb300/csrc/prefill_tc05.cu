@@ -9,16 +9,18 @@
 //
 // One CTA computes 256 query rows (two tiles of 128, the MMA's M) of one query head
 // against the key/value blocks of 128 tokens of its KV head up to the diagonal:
-//   warp 0       TMA producer: K and V blocks into a ring of NS stages in the order the
-//                MMA warp uses them (K0, V0, K1, V1, ...); zeroes the value rows past the
-//                prompt in the last block, so that P = 0 never meets a NaN;
+//   warp 0       TMA producer: the query tiles that lie inside the prompt (thread 0,
+//                at setup), then K and V blocks into a ring of NS stages in the order
+//                the MMA warp uses them (K0, V0, K1, V1, ...); zeroes the value rows past
+//                the prompt in the last block, so that P = 0 never meets a NaN;
 //   warp 1       MMA issuer (one thread): S_t = Q_t K_j^T (SS form, both K-major) and
 //                O_t += P_t V_j (TS form: P from tensor memory, V N-major in shared
 //                memory), tiles interleaved so that one tile's softmax overlaps the other
 //                tile's MMAs;
 //   warp 2       allocates and frees the 512 tensor-memory columns;
 //   warps 4..7   softmax of query tile 0, warps 8..11 of tile 1 (thread = query row):
-//                load the tile's Q rows into shared memory, then per key block read S
+//                load the tile's Q rows into shared memory when the tile reaches past
+//                the prompt (zeros there), then per key block read S
 //                (a max pass and an exponential pass over 32-column chunks), mask the
 //                diagonal block, update the running max, write P = exp2(S' - m) as fp16
 //                over the first half of S's columns, and at the end normalise O and write
@@ -211,7 +213,7 @@ __device__ __forceinline__ float row_exp_store(uint32_t t_s, float qs, float nm,
 template <int D>
 __global__ void __launch_bounds__(kTThreads, 1)
 prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                    const PrefillParams p, int nqb) {
+                    const __grid_constant__ CUtensorMap tq, const PrefillParams p, int nqb) {
   using C = TcCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t sm_raw[];
@@ -246,8 +248,12 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // A query tile whose 128 rows all lie inside the prompt comes in by one TMA box (the
+  // box never reaches past the prompt, so past the end of q); a partial or empty tile is
+  // loaded row by row by its softmax threads, with zeros past the prompt.
+  const bool q_tma[2] = {q0 + kQRows <= L, q0 + 2 * kQRows <= L};
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 2 * kQRows);
+    mbar_init(&bars->q_full, (q_tma[0] ? 1 : kQRows) + (q_tma[1] ? 1 : kQRows));
     mbar_init(&bars->v_fixed, 1);
     mbar_init(&bars->mma_final, 1);
     for (int s = 0; s < NS; ++s) {
@@ -261,6 +267,13 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     }
     bars->abort = 0;
     fence_barrier_init();
+    // the full query tiles, issued before the setup barrier (this thread initialised
+    // q_full; the copies overlap the tensor-memory allocation)
+    for (int t = 0; t < 2; ++t) {
+      if (!q_tma[t]) continue;
+      mbar_arrive_expect_tx(&bars->q_full, C::QB);
+      tma_load_4d(sQ + t * C::QB, &tq, 0, row0 + q0 + t * kQRows, 0, hq, &bars->q_full);
+    }
   }
   if (warp == 2) tc05::tmem_alloc(&bars->tmem_base, 512);
   tc05::fence_before_sync();
@@ -306,10 +319,15 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
       }
     }
     if (!ok && lane == 0) give_up(p.err, abort);
-    // the copies still in flight land before the CTA can exit
+    // the copies still in flight land before the CTA can exit (the query tiles too)
     for (int v = u > NS ? u - NS : 0; v < u; ++v) {
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(&bars->kv_full[v % NS], (v / NS) & 1) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+      }
+    }
+    if (lane == 0 && (q_tma[0] || q_tma[1])) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&bars->q_full, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
       }
     }
   } else if (warp == 1) {
@@ -415,8 +433,9 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     const uint32_t lanebase = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int prow = q0 + t * kQRows + r;                 // this thread's query position
     const int nmine = t == 0 ? nt0 : nt1;
-    // Q row -> shared memory in the 128B-swizzled K-major layout (zeros past the prompt)
-    {
+    // Q row -> shared memory in the 128B-swizzled K-major layout (zeros past the prompt),
+    // for a tile that does not come in by TMA
+    if (!q_tma[t]) {
       uint8_t* dst = sQ + t * C::QB + r * 128;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row0 + prow) * p.Hq + hq) * D);
       const bool valid = nmine > 0 && prow < L;
@@ -506,13 +525,14 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
   }
 }
 
-// 4-D view (d mod 64, token, d / 64, KV head) of the workspace [W][16][Hkv][D] fp16; the
-// box {64, 128, D/64, 1} lands one key/value block as [D/64][128 rows][128 B], 128B swizzle.
-static bool encode_ws_map(CUtensorMap* tm, const void* base, int D, int Hkv, int num_pages) {
+// 4-D view (d mod 64, row, d / 64, head) of an fp16 [rows][heads][D] array; the box
+// {64, 128, D/64, 1} lands 128 rows of one head as [D/64][128 rows][128 B], 128B swizzle:
+// a key/value block of the workspace ([W][16][Hkv][D], rows = W * 16) or a query tile.
+static bool encode_rows_map(CUtensorMap* tm, const void* base, int D, int heads, cuuint64_t rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[4] = {64, (cuuint64_t)num_pages * kPage, (cuuint64_t)(D / 64), (cuuint64_t)Hkv};
-  cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, 128, (cuuint64_t)D * 2};
+  cuuint64_t dims[4] = {64, rows, (cuuint64_t)(D / 64), (cuuint64_t)heads};
+  cuuint64_t strides[3] = {(cuuint64_t)heads * D * 2, 128, (cuuint64_t)D * 2};
   cuuint32_t box[4] = {64, (cuuint32_t)kKB, (cuuint32_t)(D / 64), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -524,8 +544,14 @@ cudaError_t set_smem_attr(const void* kern, int bytes);
 
 template <int D>
 static cudaError_t launch_tc05_d(const PrefillParams& p, int max_len, cudaStream_t st) {
-  CUtensorMap tk, tv;
-  if (!encode_ws_map(&tk, p.ws_k, D, p.Hkv, p.num_ws_pages) || !encode_ws_map(&tv, p.ws_v, D, p.Hkv, p.num_ws_pages))
+  CUtensorMap tk, tv, tq;
+  const cuuint64_t ws_rows = (cuuint64_t)p.num_ws_pages * kPage;
+  // The query rows: the host does not know T = cu_seqlens[n], so the map spans every row
+  // index a prompt can have (the device checks bound the boxes: a box is issued only for
+  // 128 rows inside one prompt, so it never reads past q's T rows).
+  const cuuint64_t q_rows = 0x7fffffffull;
+  if (!encode_rows_map(&tk, p.ws_k, D, p.Hkv, ws_rows) || !encode_rows_map(&tv, p.ws_v, D, p.Hkv, ws_rows) ||
+      !encode_rows_map(&tq, p.q, D, p.Hq, q_rows))
     return cudaErrorInvalidValue;
   const int smem = tc_smem_bytes<D>();
   cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(prefill_tc05_kernel<D>), smem);
@@ -533,7 +559,7 @@ static cudaError_t launch_tc05_d(const PrefillParams& p, int max_len, cudaStream
   const int nqb = (max_len + 2 * kQRows - 1) / (2 * kQRows);
   const long long grid = (long long)nqb * p.Hq * p.n;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_tc05_kernel<D><<<(unsigned)grid, kTThreads, smem, st>>>(tk, tv, p, nqb);
+  prefill_tc05_kernel<D><<<(unsigned)grid, kTThreads, smem, st>>>(tk, tv, tq, p, nqb);
   return cudaGetLastError();
 }
 

@@ -84,6 +84,19 @@ def test_tile_boundaries_every_row(ekv_lib, torch_cuda, D, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("lens", [[512], [256, 384], [128, 100, 256]])
+def test_query_tiles_ending_at_the_last_row(ekv_lib, torch_cuda, lens, variant):
+    # a 128-row query tile inside its prompt comes in by one TMA box; here the last prompt
+    # ends on a tile boundary, so the last box ends exactly at q's last row
+    H_q, H_kv, D = 8, 2, 128
+    q, k, v, cu, po = _case(lens, H_q, H_kv, D, 190 + len(lens))
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D, variant=variant)
+    assert err == (0, 0)
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
+    _check(out, lse, ref_out, ref_lse, np.arange(q.shape[0]))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("D", [64, 128])
 def test_growing_scores_rebase_the_max(ekv_lib, torch_cuda, D, variant):
     # keys grow along the prompt, so each row's running max climbs by many powers of two
