@@ -7,24 +7,28 @@
 // prefix). Prompt i's queries are rows cu_seqlens[i] .. of q; its keys and values are
 // workspace pages page_off[i], page_off[i] + 1, ... ([W][16][Hkv][D]).
 //
-// One CTA computes 256 query rows (two tiles of 128, the MMA's M) of one query head
-// against the key/value blocks of 128 tokens of its KV head up to the diagonal:
-//   warp 0       TMA producer: the query tiles that lie inside the prompt (thread 0,
-//                at setup), then K and V blocks into a ring of NS stages in the order
-//                the MMA warp uses them (K0, V0, K1, V1, ...); zeroes the value rows past
-//                the prompt in the last block, so that P = 0 never meets a NaN;
+// Work item = 256 query rows (two tiles of 128, the MMA's M) of one query head against
+// the key/value blocks of 128 tokens of its KV head up to the diagonal. The kernel is
+// persistent: one CTA per SM takes the items in a fixed order (heavier query blocks
+// first, dealt in a snake over the CTAs), keeps its barriers and tensor memory across
+// them, and overlaps one item's epilogue with the next item's loads and first S.
+//   warp 0       TMA producer: per item, each active query tile once the tile's previous
+//                rows have been read by their last S (one box when the 128 rows end inside
+//                q; else rows by plain loads, zeros past the prompt), then K and V blocks
+//                into a ring of NS stages in the order the MMA warp uses them (K0, V0,
+//                K1, V1, ...); zeroes the value rows past the prompt in an item's last
+//                block, so that P = 0 never meets a NaN;
 //   warp 1       MMA issuer (one thread): S_t = Q_t K_j^T (SS form, both K-major) and
 //                O_t += P_t V_j (TS form: P from tensor memory, V N-major in shared
 //                memory), tiles interleaved so that one tile's softmax overlaps the other
-//                tile's MMAs;
+//                tile's MMAs; an item's first O_t += P V waits until the softmax has read
+//                the previous item's O_t out;
 //   warp 2       allocates and frees the 512 tensor-memory columns;
 //   warps 4..7   softmax of query tile 0, warps 8..11 of tile 1 (thread = query row):
-//                load the tile's Q rows into shared memory when the tile reaches past
-//                the prompt (zeros there), then per key block read S
-//                (a max pass and an exponential pass over 32-column chunks), mask the
-//                diagonal block, update the running max, write P = exp2(S' - m) as fp16
-//                over the first half of S's columns, and at the end normalise O and write
-//                out and lse.
+//                per key block read S (a max pass and an exponential pass over 32-column
+//                chunks), mask the diagonal block, update the running max, write
+//                P = exp2(S' - m) as fp16 over the first half of S's columns, and at the
+//                end of an item normalise O and write out and lse.
 // Tensor memory, tile t: S/P at 256t (128 columns), O at 256t + 128 (D fp32 columns).
 // The MMA warp issues S of block j + 1 over P of block j right behind O += P_j V_j (the
 // tensor core runs one thread's MMAs in issue order, so P_j is read before S_{j+1}
@@ -67,14 +71,16 @@ struct TcCfg {
 
 template <int NS>
 struct TcBars {
-  uint64_t q_full;               // 256 arrivals: both tiles' Q rows in shared memory
-  uint64_t v_fixed;              // last value block with its rows past the prompt zeroed
+  uint64_t q_full[2];            // [tile]: the tile's query rows of its next work item landed
+  uint64_t q_empty[2];           // [tile]: an item's last S has read the tile's query rows
+  uint64_t v_raw;                // a last value block reaching past its prompt landed (producer)
   uint64_t mma_final;            // every MMA issued has completed
-  uint64_t kv_full[NS];          // TMA bytes landed
+  uint64_t kv_full[NS];          // TMA bytes landed (a last value block: and its tail zeroed)
   uint64_t kv_empty[NS];         // the MMAs reading the stage have completed
   uint64_t s_full[2];            // [tile]: S of the next block written
   uint64_t p_full[2];            // [tile]: P written, S read (one arrival per softmax warp)
-  uint64_t pv_done[2];           // [tile]: the tile's last O += P V completed (one phase)
+  uint64_t pv_done[2];           // [tile]: a work item's last O += P V completed
+  uint64_t o_free[2];            // [tile]: an item's O read out (one arrival per softmax warp)
   uint32_t tmem_base;
   int abort;
 };
@@ -210,6 +216,53 @@ __device__ __forceinline__ float row_exp_store(uint32_t t_s, float qs, float nm,
 
 }  // namespace
 
+// One work item: 256 query rows (two tiles of 128) of one query head of one prompt.
+struct WorkItem {
+  int row0, L, q0, hq, h, pg0;
+  int nt0, nt1, n;     // key blocks of tile 0 / tile 1 / either
+  int zr;              // value rows >= zr of the last block lie past the prompt
+  bool valid;
+};
+
+// Work item w: heavier query blocks first (w / (Hq n) counts the query blocks down), then
+// prompt, then query head. Every role of a CTA computes the same items; with `report` the
+// prompt's errors are recorded (once per prompt: at its last / first query block).
+__device__ __forceinline__ WorkItem work_item(const PrefillParams& p, int nqb, int w, bool report) {
+  WorkItem it;
+  const int HqN = p.Hq * p.n;
+  const int qb = nqb - 1 - w / HqN;
+  const int i = (w % HqN) / p.Hq;
+  it.hq = w % p.Hq;
+  it.row0 = __ldg(p.cu_seqlens + i);
+  const int len = __ldg(p.cu_seqlens + i + 1) - it.row0;
+  if (report && qb == nqb - 1 && len > p.max_len)              // reported, rows cut there
+    report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_SEQ_LEN, i);
+  it.L = min(len, p.max_len);
+  it.q0 = qb * 2 * kQRows;
+  it.h = it.hq / p.G;
+  it.pg0 = __ldg(p.page_off + i);
+  it.valid = it.q0 < it.L;
+  if (it.valid && (it.pg0 < 0 || it.pg0 + (it.L + kPage - 1) / kPage > p.num_ws_pages)) {
+    if (report && qb == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, i);
+    it.valid = false;
+  }
+  // key blocks each tile needs: up to its own (diagonal) block, and not past the prompt
+  const int nkb = (it.L + kKB - 1) / kKB;
+  it.nt0 = min(it.q0 / kKB + 1, nkb);
+  it.nt1 = it.q0 + kQRows < it.L ? min(it.q0 / kKB + 2, nkb) : 0;
+  it.n = max(it.nt0, it.nt1);
+  it.zr = it.L - (it.n - 1) * kKB;
+  return it;
+}
+
+// The r-th work item of this CTA: items are dealt in rounds of gridDim.x, alternately
+// forwards and backwards (a snake), which balances a list sorted from heavy to light about
+// as well as greedy assignment. An index >= the item count means no r-th item.
+__device__ __forceinline__ int item_index(int r) {
+  const int g = (int)gridDim.x, c = (int)blockIdx.x;
+  return r * g + ((r & 1) ? g - 1 - c : c);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTThreads, 1)
 prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -217,30 +270,7 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
   using C = TcCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t sm_raw[];
-  // ---- which 256 query rows: heavier query blocks first, then prompt, then query head
-  const int HqN = p.Hq * p.n;
-  const int qb = nqb - 1 - (int)(blockIdx.x / HqN);
-  const int i = (int)(blockIdx.x % HqN) / p.Hq, hq = (int)(blockIdx.x % p.Hq);
-  const int row0 = __ldg(p.cu_seqlens + i);
-  const int len = __ldg(p.cu_seqlens + i + 1) - row0;
-  if (qb == nqb - 1 && threadIdx.x == 0 && len > p.max_len)        // reported, rows cut there
-    report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_SEQ_LEN, i);
-  const int L = min(len, p.max_len);
-  const int q0 = qb * 2 * kQRows;
-  if (q0 >= L) return;
-  const int h = hq / p.G;
-  const int pg0 = __ldg(p.page_off + i);
-  if (pg0 < 0 || pg0 + (L + kPage - 1) / kPage > p.num_ws_pages) {
-    if (threadIdx.x == 0 && qb == 0) report_error(p.err, EKV_ERR_DEVICE_CHECK, EKV_DETAIL_PAGE_ID, i);
-    return;
-  }
-  // key blocks each tile needs: up to its own (diagonal) block, and not past the prompt
-  const int nkb = (L + kKB - 1) / kKB;
-  const int nt0 = min(q0 / kKB + 1, nkb);
-  const int nt1 = q0 + kQRows < L ? min(q0 / kKB + 2, nkb) : 0;
-  const int n = max(nt0, nt1);
-  const int zr = L - (n - 1) * kKB;          // value rows >= zr of the last block are zeroed
-
+  const int W = nqb * p.Hq * p.n;                         // work items
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;                                     // [2][NB][128 rows][128 B]
   uint8_t* sKV = base + 2 * C::QB;                        // [NS][NB][128 rows][128 B]
@@ -248,32 +278,23 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // A query tile whose 128 rows all lie inside the prompt comes in by one TMA box (the
-  // box never reaches past the prompt, so past the end of q); a partial or empty tile is
-  // loaded row by row by its softmax threads, with zeros past the prompt.
-  const bool q_tma[2] = {q0 + kQRows <= L, q0 + 2 * kQRows <= L};
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, (q_tma[0] ? 1 : kQRows) + (q_tma[1] ? 1 : kQRows));
-    mbar_init(&bars->v_fixed, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->q_full[t], 1);
+      mbar_init(&bars->q_empty[t], 1);
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], kQRows / 32);
+      mbar_init(&bars->pv_done[t], 1);
+      mbar_init(&bars->o_free[t], kQRows / 32);
+    }
+    mbar_init(&bars->v_raw, 1);
     mbar_init(&bars->mma_final, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], kQRows / 32);
-      mbar_init(&bars->pv_done[t], 1);
-    }
     bars->abort = 0;
     fence_barrier_init();
-    // the full query tiles, issued before the setup barrier (this thread initialised
-    // q_full; the copies overlap the tensor-memory allocation)
-    for (int t = 0; t < 2; ++t) {
-      if (!q_tma[t]) continue;
-      mbar_arrive_expect_tx(&bars->q_full, C::QB);
-      tma_load_4d(sQ + t * C::QB, &tq, 0, row0 + q0 + t * kQRows, 0, hq, &bars->q_full);
-    }
   }
   if (warp == 2) tc05::tmem_alloc(&bars->tmem_base, 512);
   tc05::fence_before_sync();
@@ -283,51 +304,97 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    const int tok0 = pg0 * kPage;
+    const int T = __ldg(p.cu_seqlens + p.n);               // rows of q
     int stage = 0, u = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, rawc = 0;
+    uint32_t ql[2] = {0u, 0u};                             // query tiles loaded, per tile
     bool ok = true;
-    for (int j = 0; ok && j < n; ++j) {
-      for (int is_v = 0; is_v < 2; ++is_v) {
-        if (u >= NS) {                                      // the stage's previous item consumed
-          ok = __all_sync(0xffffffffu, wait_bar(&bars->kv_empty[stage], phase ^ 1u, abort));
+    for (int r = 0; ok && item_index(r) < W; ++r) {
+      const WorkItem it = work_item(p, nqb, item_index(r), lane == 0);
+      if (!it.valid) continue;
+      // The item's query tiles, each once the tile's previous rows have been read by their
+      // last S. One TMA box when the 128 rows end inside q (rows past the prompt then
+      // belong to the next prompt: they are computed, never stored); else rows by plain
+      // loads with zeros past the prompt.
+      for (int t = 0; t < 2 && ok; ++t) {
+        if ((t == 0 ? it.nt0 : it.nt1) == 0) continue;
+        if (ql[t] > 0) {
+          ok = __all_sync(0xffffffffu, wait_bar(&bars->q_empty[t], (ql[t] - 1u) & 1u, abort));
           if (!ok) break;
         }
-        uint8_t* dst = sKV + stage * C::IB;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->kv_full[stage], C::IB);
-          tma_load_4d(dst, is_v ? &tv : &tk, 0, tok0 + j * kKB, 0, h, &bars->kv_full[stage]);
-        }
-        if (is_v && j == n - 1 && zr < kKB) {
-          ok = __all_sync(0xffffffffu, wait_bar(&bars->kv_full[stage], phase, abort));
-          if (!ok) break;
-          const int per_slab = (kKB - zr) * 8;             // 16-byte chunks past the prompt
-          for (int e = lane; e < per_slab * C::NB; e += 32) {
-            const int slab = e / per_slab, rem = e % per_slab;
-            *reinterpret_cast<uint4*>(dst + slab * kKB * 128 + (zr + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+        const int rq = it.row0 + it.q0 + t * kQRows;
+        uint8_t* dq = sQ + t * C::QB;
+        if (rq + kQRows <= T) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars->q_full[t], C::QB);
+            tma_load_4d(dq, &tq, 0, rq, 0, it.hq, &bars->q_full[t]);
+          }
+        } else {
+          for (int e = lane; e < kQRows * (D / 8); e += 32) {
+            const int rr = e / (D / 8), c = e % (D / 8);
+            const bool valid = it.q0 + t * kQRows + rr < it.L;
+            const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)(rq + rr) * p.Hq + it.hq) * D) + c)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(dq + (c >> 3) * (kQRows * 128) + rr * 128 + (((c & 7) ^ (rr & 7)) << 4)) = v;
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->v_fixed);
+          if (lane == 0) mbar_arrive(&bars->q_full[t]);
         }
-        ++u;
-        if (++stage == NS) {
-          stage = 0;
-          phase ^= 1u;
+        ++ql[t];
+      }
+      if (!ok) break;
+      const int tok0 = it.pg0 * kPage;
+      for (int j = 0; ok && j < it.n; ++j) {
+        for (int is_v = 0; is_v < 2; ++is_v) {
+          if (u >= NS) {                                    // the stage's previous item consumed
+            ok = __all_sync(0xffffffffu, wait_bar(&bars->kv_empty[stage], phase ^ 1u, abort));
+            if (!ok) break;
+          }
+          uint8_t* dst = sKV + stage * C::IB;
+          if (is_v && j == it.n - 1 && it.zr < kKB) {
+            // the last value block reaches past the prompt: it lands on v_raw, its rows past
+            // the prompt are zeroed (so that P = 0 never meets a NaN), then the stage is
+            // published on kv_full by a plain arrival
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&bars->v_raw, C::IB);
+              tma_load_4d(dst, &tv, 0, tok0 + j * kKB, 0, it.h, &bars->v_raw);
+            }
+            ok = __all_sync(0xffffffffu, wait_bar(&bars->v_raw, rawc & 1u, abort));
+            ++rawc;
+            if (!ok) break;
+            const int per_slab = (kKB - it.zr) * 8;         // 16-byte chunks past the prompt
+            for (int e = lane; e < per_slab * C::NB; e += 32) {
+              const int slab = e / per_slab, rem = e % per_slab;
+              *reinterpret_cast<uint4*>(dst + slab * kKB * 128 + (it.zr + rem / 8) * 128 + (rem % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->kv_full[stage]);
+          } else if (lane == 0) {
+            mbar_arrive_expect_tx(&bars->kv_full[stage], C::IB);
+            tma_load_4d(dst, is_v ? &tv : &tk, 0, tok0 + j * kKB, 0, it.h, &bars->kv_full[stage]);
+          }
+          ++u;
+          if (++stage == NS) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
     if (!ok && lane == 0) give_up(p.err, abort);
-    // the copies still in flight land before the CTA can exit (the query tiles too)
+    // the copies still in flight land before the CTA can exit
     for (int v = u > NS ? u - NS : 0; v < u; ++v) {
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(&bars->kv_full[v % NS], (v / NS) & 1) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
       }
     }
-    if (lane == 0 && (q_tma[0] || q_tma[1])) {
+    for (int t = 0; t < 2; ++t) {
+      if (ql[t] == 0) continue;
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&bars->q_full, 0) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
+      while (!mbar_try_wait(&bars->q_full[t], (ql[t] - 1u) & 1u) && globaltimer_ns() - t0 < kWaitTimeoutNs) {
       }
     }
   } else if (warp == 1) {
@@ -337,14 +404,15 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     constexpr uint32_t idS = tc05::idesc_f16_f32(kQRows, kKB, false);
     constexpr uint32_t idO = tc05::idesc_f16_f32(kQRows, D, true);
     constexpr uint32_t HI = tc05::sdesc_hi(1024);          // 8-row groups 1024 B apart
-    const int nt[2] = {nt0, nt1};
     // descriptor low words: Q tile 0, K-major and V (N-major) views of ring stage 0
     const uint32_t q_lo = tc05::sdesc_lo(smem_u32(sQ), 16);
     const uint32_t k_lo = tc05::sdesc_lo(smem_u32(sKV), 16);
     const uint32_t v_lo = tc05::sdesc_lo(smem_u32(sKV), kKB * 128);
-    // ring cursors of the K items (2j) and the V items (2j + 1)
+    // ring cursors of the K items (2j) and the V items (2j + 1) of each work item
     int ks = 0, vs = 1;
     uint32_t kp = 0, vp = 0;
+    // phases taken so far: q_full[t], p_full[t]; items with an O of tile t (o_free phases)
+    uint32_t qc[2] = {0u, 0u}, pc[2] = {0u, 0u}, oc[2] = {0u, 0u};
     auto adv2 = [&](int& s, uint32_t& ph) {
       s += 2;
       if (s >= NS) {
@@ -371,54 +439,74 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
       if (tc05::elect_one()) tc05::commit(bar);
       __syncwarp();
     };
-    bool ok = wait_all(&bars->q_full, 0) && wait_all(&bars->kv_full[ks], kp);
-    if (ok) {
-      tc05::fence_after_sync();
-      for (int t = 0; t < 2; ++t)
-        if (nt[t] > 0) issue_s(t);
-      commit_one(&bars->kv_empty[ks]);
-      adv2(ks, kp);
-    }
-    for (int j = 0; ok && j < n; ++j) {
-      ok = (j == n - 1 && zr < kKB) ? wait_all(&bars->v_fixed, 0) : wait_all(&bars->kv_full[vs], vp);
-      if (!ok) break;
-      tc05::fence_after_sync();
-      const uint32_t va = v_lo + vs * (C::IB >> 4);
-      bool k_ready = false;
+    bool ok = true;
+    for (int r = 0; ok && item_index(r) < W; ++r) {
+      const WorkItem it = work_item(p, nqb, item_index(r), false);
+      if (!it.valid) continue;
+      const int nt[2] = {it.nt0, it.nt1}, n = it.n;
+      ok = wait_all(&bars->kv_full[ks], kp);
+      // S of the first block for each active tile, once its query rows are in. The tile's
+      // S columns hold the previous item's last P until its O += P V, issued before, has
+      // read it (one thread's MMAs run in issue order).
       for (int t = 0; t < 2 && ok; ++t) {
-        if (j >= nt[t]) continue;
-        // O_t += P_t V_j once the softmax has written P
-        ok = wait_all(&bars->p_full[t], j & 1);
+        if (nt[t] == 0) continue;
+        ok = wait_all(&bars->q_full[t], qc[t] & 1u);
+        ++qc[t];
         if (!ok) break;
         tc05::fence_after_sync();
-        const uint32_t pa = tbase + t * 256, od = tbase + t * 256 + 128;
-        const bool acc0 = j > 0;
-        if (tc05::elect_one()) {
-#pragma unroll
-          for (int k = 0; k < kKB / 16; ++k)
-            tc05::mma_ts(od, pa + 8 * k, tc05::sdesc_join(va + k * (2048 >> 4), HI), idO, acc0 || k > 0);
-          if (j + 1 == nt[t]) tc05::commit(&bars->pv_done[t]);   // the tile's last O += P V
-        }
-        __syncwarp();
-        if (j + 1 < nt[t]) {
-          // S_t of block j + 1 overwrites P_t. It is issued at once, behind O_t += P_t V_j:
-          // the tensor core runs the MMAs of this thread in issue order, so P_t is read
-          // before it is overwritten, and the commit after S_t (s_full) arrives only
-          // once every MMA issued before it, O_t += P_t V_j included, has completed.
-          ok = k_ready || wait_all(&bars->kv_full[ks], kp);
-          if (!ok) break;
-          k_ready = true;
-          tc05::fence_after_sync();
-          issue_s(t);
-        }
+        issue_s(t);
+        if (nt[t] == 1) commit_one(&bars->q_empty[t]);    // the tile's last S of the item
       }
       if (!ok) break;
-      commit_one(&bars->kv_empty[vs]);
-      adv2(vs, vp);
-      if (j + 1 < n) {
-        commit_one(&bars->kv_empty[ks]);
-        adv2(ks, kp);
+      commit_one(&bars->kv_empty[ks]);
+      adv2(ks, kp);
+      for (int j = 0; ok && j < n; ++j) {
+        ok = wait_all(&bars->kv_full[vs], vp);
+        if (!ok) break;
+        tc05::fence_after_sync();
+        const uint32_t va = v_lo + vs * (C::IB >> 4);
+        bool k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nt[t]) continue;
+          // O_t += P_t V_j once the softmax has written P (and, for the first block, once
+          // the previous item's O_t has been read out: this product overwrites it)
+          ok = wait_all(&bars->p_full[t], pc[t] & 1u);
+          ++pc[t];
+          if (ok && j == 0 && oc[t] > 0) ok = wait_all(&bars->o_free[t], (oc[t] - 1u) & 1u);
+          if (!ok) break;
+          tc05::fence_after_sync();
+          const uint32_t pa = tbase + t * 256, od = tbase + t * 256 + 128;
+          const bool acc0 = j > 0;
+          if (tc05::elect_one()) {
+#pragma unroll
+            for (int k = 0; k < kKB / 16; ++k)
+              tc05::mma_ts(od, pa + 8 * k, tc05::sdesc_join(va + k * (2048 >> 4), HI), idO, acc0 || k > 0);
+            if (j + 1 == nt[t]) tc05::commit(&bars->pv_done[t]);   // the item's last O_t += P V
+          }
+          __syncwarp();
+          if (j + 1 < nt[t]) {
+            // S_t of block j + 1 overwrites P_t. It is issued at once, behind O_t += P_t V_j:
+            // the tensor core runs the MMAs of this thread in issue order, so P_t is read
+            // before it is overwritten, and the commit after S_t (s_full) arrives only
+            // once every MMA issued before it, O_t += P_t V_j included, has completed.
+            ok = k_ready || wait_all(&bars->kv_full[ks], kp);
+            if (!ok) break;
+            k_ready = true;
+            tc05::fence_after_sync();
+            issue_s(t);
+            if (j + 2 == nt[t]) commit_one(&bars->q_empty[t]);   // the tile's last S of the item
+          }
+        }
+        if (!ok) break;
+        commit_one(&bars->kv_empty[vs]);
+        adv2(vs, vp);
+        if (j + 1 < n) {
+          commit_one(&bars->kv_empty[ks]);
+          adv2(ks, kp);
+        }
       }
+      for (int t = 0; t < 2; ++t)
+        if (nt[t] > 0) ++oc[t];
     }
     if (!ok && lane == 0) give_up(p.err, abort);
     commit_one(&bars->mma_final);
@@ -431,78 +519,71 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
     // ------------------------------------------------------- softmax, tile t
     const int t = (warp - 4) >> 2, r = threadIdx.x - 128 - t * kQRows;
     const uint32_t lanebase = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int prow = q0 + t * kQRows + r;                 // this thread's query position
-    const int nmine = t == 0 ? nt0 : nt1;
-    // Q row -> shared memory in the 128B-swizzled K-major layout (zeros past the prompt),
-    // for a tile that does not come in by TMA
-    if (!q_tma[t]) {
-      uint8_t* dst = sQ + t * C::QB + r * 128;
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)(row0 + prow) * p.Hq + hq) * D);
-      const bool valid = nmine > 0 && prow < L;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(dst + (c >> 3) * (kQRows * 128) + (((c & 7) ^ (r & 7)) << 4)) = v;
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&bars->q_full);
-    }
     const float qs = p.qscale;
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
     const uint32_t t_s = tbase + t * 256 + lanebase, t_o = tbase + t * 256 + 128 + lanebase;
-    for (int j = 0; j < nmine; ++j) {
-      // S of block j is ready; O += P V of block j - 1 has completed too (the commit that
-      // signals S was issued after it)
-      ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full[t], j & 1, abort));
+    uint32_t sc = 0, pvc = 0;                              // phases taken: s_full, pv_done
+    bool ok = true;
+    for (int ri = 0; ok && item_index(ri) < W; ++ri) {
+      const WorkItem it = work_item(p, nqb, item_index(ri), false);
+      const int nmine = !it.valid ? 0 : (t == 0 ? it.nt0 : it.nt1);
+      if (nmine == 0) continue;
+      const int prow = it.q0 + t * kQRows + r;             // this thread's query position
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < nmine; ++j) {
+        // S of block j is ready; O += P V of block j - 1 has completed too (the commit that
+        // signals S was issued after it)
+        ok = __all_sync(0xffffffffu, wait_bar(&bars->s_full[t], sc & 1u, abort));
+        ++sc;
+        if (!ok) break;
+        tc05::fence_after_sync();
+        const int k0 = j * kKB;
+        const bool diag = k0 + kKB - 1 > it.q0 + t * kQRows;   // the block reaches past some row
+        uint32_t sv[4][32];
+        const float mx = diag ? row_in_regs<true>(t_s, k0, prow, sv) : row_in_regs<false>(t_s, k0, prow, sv);
+        const float m_new = fmaxf(m_ref, mx * qs);
+        const bool need = m_new > m_ref + kRebase;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2f(m_ref - m_new) : 1.f;
+          // O holds blocks < j, all complete (S of this block was committed after them)
+          if (j > 0) {
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t o[16];
+              tld16(t_o + 16 * c, o);
+              tc05::wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tst16(t_o + 16 * c, o);
+            }
+          }
+          l *= alpha;
+          if (need) m_ref = m_new;
+        }
+        l += row_exp_store(t_s, qs, -m_ref, sv);
+        tc05::wait_st();
+        tc05::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[t]);      // one arrival per warp
+      }
+      if (!ok) break;
+      // the item's last O += P V (its commit covers every earlier MMA)
+      ok = __all_sync(0xffffffffu, wait_bar(&bars->pv_done[t], pvc & 1u, abort));
+      ++pvc;
       if (!ok) break;
       tc05::fence_after_sync();
-      const int k0 = j * kKB;
-      const bool diag = k0 + kKB - 1 > q0 + t * kQRows;   // the block reaches past some row
-      uint32_t sv[4][32];
-      const float mx = diag ? row_in_regs<true>(t_s, k0, prow, sv) : row_in_regs<false>(t_s, k0, prow, sv);
-      const float m_new = fmaxf(m_ref, mx * qs);
-      const bool need = m_new > m_ref + kRebase;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ex2f(m_ref - m_new) : 1.f;
-        // O holds blocks < j, all complete (S of this block was committed after them)
-        if (j > 0) {
-#pragma unroll 1
-          for (int c = 0; c < D / 16; ++c) {
-            uint32_t o[16];
-            tld16(t_o + 16 * c, o);
-            tc05::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tst16(t_o + 16 * c, o);
-          }
-        }
-        l *= alpha;
-        if (need) m_ref = m_new;
-      }
-      l += row_exp_store(t_s, qs, -m_ref, sv);
-      tc05::wait_st();
-      tc05::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[t]);      // one arrival per warp
-    }
-    if (!ok && lane == 0) give_up(p.err, abort);
-    if (ok && nmine > 0) {
-      // the last O += P V of the tile (its commit, the only one on pv_done, covers every
-      // earlier MMA)
-      ok = __all_sync(0xffffffffu, wait_bar(&bars->pv_done[t], 0, abort));
-      if (!ok && lane == 0) give_up(p.err, abort);
-    }
-    if (ok && nmine > 0) {
-      tc05::fence_after_sync();
       const float inv = 1.f / l;
-      __half* dst = p.out + ((size_t)(row0 + prow) * p.Hq + hq) * D;
+      __half* dst = p.out + ((size_t)(it.row0 + prow) * p.Hq + it.hq) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tc05::ld32(t_o + 32 * c, o);
         tc05::wait_ld();
-        if (prow < L) {
+        if (c == D / 32 - 1) {                             // O read out: the next item may overwrite it
+          tc05::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->o_free[t]);
+        }
+        if (prow < it.L) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 w;
@@ -514,8 +595,10 @@ prefill_tc05_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constan
           }
         }
       }
-      if (prow < L && p.lse) p.lse[(size_t)(row0 + prow) * p.Hq + hq] = (m_ref + log2f(l)) * 0.69314718055994531f;
+      if (prow < it.L && p.lse)
+        p.lse[(size_t)(it.row0 + prow) * p.Hq + it.hq] = (m_ref + log2f(l)) * 0.69314718055994531f;
     }
+    if (!ok && lane == 0) give_up(p.err, abort);
   }
   tc05::fence_before_sync();
   __syncthreads();
@@ -557,9 +640,14 @@ static cudaError_t launch_tc05_d(const PrefillParams& p, int max_len, cudaStream
   cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(prefill_tc05_kernel<D>), smem);
   if (e != cudaSuccess) return e;
   const int nqb = (max_len + 2 * kQRows - 1) / (2 * kQRows);
-  const long long grid = (long long)nqb * p.Hq * p.n;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_tc05_kernel<D><<<(unsigned)grid, kTThreads, smem, st>>>(tk, tv, tq, p, nqb);
+  const long long items = (long long)nqb * p.Hq * p.n;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)(items < sms ? items : sms);        // persistent: one CTA per SM
+  prefill_tc05_kernel<D><<<grid, kTThreads, smem, st>>>(tk, tv, tq, p, nqb);
   return cudaGetLastError();
 }
 
