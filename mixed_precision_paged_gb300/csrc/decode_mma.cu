@@ -95,6 +95,8 @@ __device__ __forceinline__ void e4m3_rows(uint32_t reg, uint32_t& row_d, uint32_
 
 // Growth of the running max (log2 units) that triggers a re-base (the weights stay < 256).
 constexpr float kRebase = 8.f;
+// Pages before a segment's end at which the next sequence's query rows are prefetched.
+constexpr int kQPrefetch = 4;
 
 template <int D, int VMODE, int EL>
 __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV8,
@@ -181,6 +183,13 @@ __device__ void consume_mma(const DecodeParams& p, const CUtensorMap* tmK, const
     bool seg_bad = false;                           // a page of this segment was skipped
     const int r_end = j1 - start;
     for (; k < r_end; ++k) {
+      // a few pages before this segment ends, the next sequence's query rows of this KV
+      // head (G x D fp16, one 128-byte line per lane) are pulled into L1, so that the
+      // next segment starts without a trip to memory
+      if (k == r_end - kQPrefetch && b < b_last && lane * 64 < G * D) {
+        const __half* qn = p.q + ((size_t)(b + 1) * p.Hq + h * G) * D + lane * 64;
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(qn));
+      }
       if ((k & 31) == 0 && k > 0) {                 // next metadata batch
         cur = nxt;
         nxt = nxt2;
