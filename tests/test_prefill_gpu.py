@@ -174,6 +174,35 @@ def test_prompt_longer_than_max_len_is_reported(ekv_lib, torch_cuda, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+def test_prompt_longer_than_max_len_first(ekv_lib, torch_cuda, variant):
+    # the cut prompt comes first: the next prompt's rows start past n * max_len
+    q, k, v, cu, po = _case([700, 40, 90], 8, 2, 128, 155)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, 8, 2, 128, max_len=256, variant=variant)
+    assert err == (ekv_lib.EKV_ERR_DEVICE_CHECK, ekv_lib.EKV_DETAIL_SEQ_LEN)
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
+    rows = np.r_[0:256, 700:830]
+    _check(out, lse, ref_out, ref_lse, rows)
+    assert np.all(np.isnan(out[256:700]))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_prompt_outside_the_workspace_is_reported(ekv_lib, torch_cuda, variant):
+    # prompt 1's pages would run past the workspace: reported (page id), its rows left
+    # untouched, the prompts before and after it computed as usual
+    lens = [100, 300, 50]
+    q, k, v, cu, po = _case(lens, 8, 2, 128, 157)
+    po = po.copy()
+    po[1] = k.shape[0] - 3                      # 19 pages from 3 before the end
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, 8, 2, 128, variant=variant)
+    assert err == (ekv_lib.EKV_ERR_DEVICE_CHECK, ekv_lib.EKV_DETAIL_PAGE_ID)
+    keep = np.r_[0:100, 400:450]
+    ref_out, ref_lse = op.prefill_attention(q[keep], k, v, np.array([0, 100, 150], np.int32),
+                                            np.array([po[0], po[2]], np.int32))
+    _check(out[keep], lse[keep], ref_out, ref_lse, np.arange(150))
+    assert np.all(np.isnan(out[100:400]))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 def test_explicit_scale_empty_prompts_and_no_lse(ekv_lib, torch_cuda, variant):
     torch = torch_cuda
     lens = [0, 37, 0, 130, 1]
