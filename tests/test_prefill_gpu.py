@@ -98,6 +98,23 @@ def test_query_tiles_ending_at_the_last_row(ekv_lib, torch_cuda, lens, variant):
 
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("D", [64, 128])
+def test_many_ragged_prompts_every_row(ekv_lib, torch_cuda, D, variant):
+    # 48 prompts of random lengths (an empty one included): many work items per CTA, items
+    # past their prompt's end, partial query tiles, the last prompt's last tile at q's end
+    rng = np.random.default_rng(200 + D)
+    lens = [int(x) for x in rng.integers(0, 700, size=48)]
+    lens[7] = 0
+    lens[-1] = 257
+    H_q, H_kv = 8, 2
+    q, k, v, cu, po = _case(lens, H_q, H_kv, D, 210 + D)
+    out, lse, err = _run(ekv_lib, torch_cuda, q, k, v, cu, po, H_q, H_kv, D, variant=variant)
+    assert err == (0, 0)
+    ref_out, ref_lse = op.prefill_attention(q, k, v, cu, po)
+    _check(out, lse, ref_out, ref_lse, np.arange(q.shape[0]))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("D", [64, 128])
 def test_growing_scores_rebase_the_max(ekv_lib, torch_cuda, D, variant):
     # keys grow along the prompt, so each row's running max climbs by many powers of two
     # across its key blocks (the lazy re-basing of O and l must run, repeatedly)
