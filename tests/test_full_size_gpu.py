@@ -12,6 +12,10 @@ workspace; ElasticKV Sec. 3.4 "Transition protocols"): the benchmark's inputs, g
 in 4 chunks of 4,096 pages into one 4,096-page workspace, and 8,192 of the 16,384 FP16
 value pages demoted; every workspace page, every code, scale and mode byte is compared
 bit for bit with the oracle, in chunks of pages so that host memory stays bounded.
+
+Prefill (8 prompts x 8192 tokens, 32/8 heads, head dim 128, the benchmark's shape): rows on
+and around the query-tile and key-block boundaries of every prompt, and random ones, every
+query head, against the float64 oracle.
 """
 
 import numpy as np
@@ -147,3 +151,38 @@ def test_demote_full_size_bit_exact(ekv_lib, torch_cuda, gather_demote_inputs):
         assert np.array_equal(got[:, n:], sub_v[:, n:])        # the second half of the slot unchanged
         assert np.array_equal(scale_out[pc].cpu().numpy().view(np.uint32), rs.view(np.uint32))
     ctx.close()
+
+
+def test_prefill_full_size_sampled_rows(ekv_lib, torch_cuda):
+    # the benchmark's prefill: 8 prompts x 8192 tokens, 32/8 heads, head dim 128, over a
+    # workspace of exactly their 4,096 pages, in the persistent tcgen05 form; rows on and
+    # around the query-tile and key-block boundaries (and random ones) of every prompt,
+    # every query head, against the float64 oracle
+    from oracle import prefill as op
+    torch = torch_cuda
+    n, L, H_q, H_kv, D = 8, 8192, 32, 8, 128
+    pages = L // 16
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1002)
+    ws_k = torch.randn((n * pages, 16, H_kv, D), generator=g, device="cuda").to(torch.float16)
+    ws_v = torch.randn((n * pages, 16, H_kv, D), generator=g, device="cuda").to(torch.float16)
+    q = torch.randn((n * L, H_q, D), generator=g, device="cuda").to(torch.float16)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full((n * L, H_q), float("nan"), dtype=torch.float32, device="cuda")
+    cu = torch.arange(0, (n + 1) * L, L, dtype=torch.int32, device="cuda")
+    po = torch.arange(0, n * pages, pages, dtype=torch.int32, device="cuda")
+    ctx = ekv_lib.Context(H_q, H_kv, D, 1)
+    ekv_lib.ekv_prefill_attention(ctx.handle, q, ws_k, ws_v, n * pages, cu, po, n, L, 0.0, out, lse)
+    torch.cuda.synchronize()
+    assert ctx.error() == (0, 0)
+    rng = np.random.default_rng(77)
+    fixed = [0, 1, 127, 128, 255, 256, 4095, 4096, 8064, 8191]
+    sample = {i: sorted(set(fixed + [int(x) for x in rng.integers(0, L, size=6)])) for i in range(n)}
+    ref_out, ref_lse = op.prefill_attention(q.cpu().numpy(), ws_k.cpu().numpy(), ws_v.cpu().numpy(),
+                                            cu.cpu().numpy(), po.cpu().numpy(), rows=sample)
+    rows = np.array([i * L + s for i, ss in sample.items() for s in ss])
+    o = out.float().cpu().numpy()[rows]
+    e = np.abs(o - ref_out[rows]).max()
+    assert e <= 2e-3, f"max-abs error {e:.3e}"
+    le = np.abs(lse.cpu().numpy()[rows] - ref_lse[rows]).max()
+    assert le <= 1e-3, f"lse error {le:.3e}"
