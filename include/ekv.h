@@ -87,7 +87,7 @@ typedef enum {
   EKV_DETAIL_SEQ_LEN = 3,        /* seq_lens[b] < 0 or > block_table_stride * 16 */
   EKV_DETAIL_NONFINITE_PAGE = 4, /* a page given to demotion holds NaN or inf */
   EKV_DETAIL_TIMEOUT = 5,        /* a bounded pipeline wait gave up */
-  EKV_DETAIL_PAGE_MODE = 6       /* a page_mode byte is neither TARGET nor COMPACT */
+  EKV_DETAIL_PAGE_MODE = 6       /* a page_mode byte is not TARGET, COMPACT or BASE */
 } ekv_detail;
 
 typedef struct ekv_ctx ekv_ctx;
