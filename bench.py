@@ -804,6 +804,18 @@ def main():
     torch.cuda.synchronize()
     split_ms, split_n = ekv.ekv_profile_read(ctx.handle)
     ekv.ekv_profile_enable(ctx.handle, False)
+    # the same launches back to back in plain stream order with no events between them:
+    # no programmatic overlap, and no event pair inside each launch's time
+    plain_ms = None
+    if flush is None:
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        plain_steps = min(args.steps, 20)
+        p0.record(stream)
+        for _ in range(plain_steps):
+            step()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        plain_ms = p0.elapsed_time(p1) / (plain_steps * layers)
     ekv.ekv_set_pdl(ctx.handle, int(pdl))
     # what the same events cost around an empty launch of the split kernel's shape
     floor_ms = ekv.ekv_profile_launch_floor(ctx.handle, 64, stream)
@@ -928,6 +940,14 @@ def main():
                                          "launch_mode": "each launch alone in plain stream order, between the "
                                                         "library's CUDA events on the launching stream (a "
                                                         "separate pass after the timed region)",
+                                         "plain_order_stream": (
+                                             {"avg_launch_ms": plain_ms,
+                                              "achieved": split_bytes / (plain_ms / 1e3) / 1e9,
+                                              "frac": split_bytes / (plain_ms / 1e3) / 1e9 / hbm,
+                                              "launch_mode": "the layer calls back to back in plain stream "
+                                                             "order (no programmatic launch), CUDA events "
+                                                             "around the pass only"}
+                                             if plain_ms else None),
                                          "launch_floor_ms": floor_ms,
                                          "launch_floor": "an empty kernel with the split kernel's grid, block, "
                                                          "shared memory and parameters, between the same "
